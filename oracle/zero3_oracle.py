@@ -1,0 +1,527 @@
+"""Plain CPU oracle of the ZeRO-3 sharded mixed-precision AdamW step.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the smoke check and by the
+benchmark's CPU-baseline leg, never by the library.  It shares no code with
+the CUDA path.
+
+What it computes, with the passages each part follows:
+
+* partition     -- flatten the parameter list, keep tensors with fewer than
+                   `threshold` elements unpartitioned, pad the flat buffer to a
+                   multiple of N_d and cut it into N_d contiguous shards;
+                   group the flat buffer into reduce buckets.
+* reduce_scatter, adamw_update, cast_bf16, allgather, sharded_step
+                -- the per-rank training step: gradient reduce-scatter, AdamW
+                   on the rank's fp32 master/m/v slice, fp32->half write-back,
+                   parameter all-gather.
+* ddp_step      -- the unsharded data-parallel step (all-reduce, then the full
+                   AdamW on every replica) that the sharded step must equal.
+* persistent_step -- the unpartitioned (persistent) group, updated DDP style.
+* fetch_submodule -- gather a submodule's shards into one contiguous tensor.
+* memory_bytes, comm_elems, ring_send_bytes -- the model-state and
+                   communication accounting.
+
+Precision: the pages fix the storage types (bf16 params and grads, fp32
+master/m/v: "ddp-to-zero-memory-sharding", 111qqz.com, section "先把账对齐").
+The update is carried out in binary32, one IEEE operation at a time with
+round-to-nearest-even and no fused multiply-add, in the fixed order written in
+`adamw_update`.  numpy float32 ufuncs perform exactly one rounded operation
+each, so every line below is one IEEE operation per element.
+
+Parity pins (tests/test_oracle_pins.py): the worked examples of the pages,
+closed forms of AdamW in float64, torch.optim.AdamW for N_d = 1, the
+sharded == DDP invariant, the accounting numbers printed on the pages, and
+brute force of the shard map on tiny lists.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+NOT_AVAILABLE, INFLIGHT, AVAILABLE = 0, 1, 2
+
+F32 = np.float32
+
+
+# --------------------------------------------------------------------------
+# partition
+# --------------------------------------------------------------------------
+@dataclass
+class Plan:
+    n_ranks: int
+    threshold: int
+    bucket: int
+    numel: List[int]
+    submodule: List[int]
+    persistent: List[bool]
+    offset: List[int]            # flat offset (partitioned) or persistent offset
+    psi_p: int                   # partitioned elements
+    psi_pad: int                 # psi_p rounded up to a multiple of n_ranks
+    shard_len: int               # S = psi_pad / n_ranks
+    psi_s: int                   # persistent elements
+    buckets: List[Tuple[int, int]]
+    segments: List[List[Tuple[int, int, int, int]]]  # (rank, shard_off, tensor_off, len)
+    submodules: Dict[int, List[int]] = field(default_factory=dict)
+
+    @property
+    def n_submodules(self) -> int:
+        return (max(self.submodules) + 1) if self.submodules else 0
+
+    def submodule_numel(self, k: int) -> int:
+        return sum(self.numel[t] for t in self.submodules.get(k, []))
+
+
+def partition(numels: Sequence[int], submodule_of: Optional[Sequence[int]], n_ranks: int,
+              threshold: int = 100_000, bucket: int = 500_000_000) -> Plan:
+    """Flatten, classify, pad and shard a parameter list.
+
+    * A tensor whose element count is strictly below the persistence
+      threshold is not partitioned and stays resident on every rank
+      ("DeepSpeed Zero-3 的参数分区与按需访问机制", hotelren.com, the
+      paragraph on 小参数驻留; ZERO tutorial, cnhsyj.com, section 3.2,
+      stage3_param_persistence_threshold "小于此大小的參數張量不會被分區").
+    * The remaining tensors are concatenated in list order into one flat
+      buffer; rank r owns the r-th contiguous 1/N_d of it (ZERO tutorial,
+      section 2.1: GPU0 keeps parameters 1..Ψ/Nd, GPU1 the next part), so a
+      shard boundary may fall inside a tensor ("ddp-to-zero-memory-sharding",
+      111qqz.com, section "ZeRO-3：参数为什么也可以分片": one layer's eight
+      weights spread over four GPUs; granularity organised by the framework).
+    * The flat buffer is zero-padded at its end to a multiple of N_d.
+    * Reduce buckets are consecutive reduce_bucket_size-element ranges of the
+      flat buffer (ZERO tutorial, sections 3.1/3.3: buckets group many small
+      reductions into a few large ones).
+    """
+    if n_ranks < 1:
+        raise ValueError("n_ranks must be >= 1")
+    if bucket < 1:
+        raise ValueError("bucket must be >= 1")
+    n = len(numels)
+    if submodule_of is None:
+        submodule_of = list(range(n))
+    persistent = [int(x) < threshold for x in numels]
+    offset = []
+    flat = 0
+    pers = 0
+    for t in range(n):
+        if persistent[t]:
+            offset.append(pers)
+            pers += int(numels[t])
+        else:
+            offset.append(flat)
+            flat += int(numels[t])
+    psi_p = flat
+    psi_pad = -(-psi_p // n_ranks) * n_ranks
+    S = psi_pad // n_ranks
+    buckets = [(lo, min(lo + bucket, psi_pad)) for lo in range(0, psi_pad, bucket)]
+    segments = []
+    for t in range(n):
+        segs = []
+        if not persistent[t]:
+            f, end = offset[t], offset[t] + int(numels[t])
+            while f < end:
+                r = f // S
+                stop = min(end, (r + 1) * S)
+                segs.append((r, f - r * S, f - offset[t], stop - f))
+                f = stop
+        segments.append(segs)
+    subs: Dict[int, List[int]] = {}
+    for t in range(n):
+        subs.setdefault(int(submodule_of[t]), []).append(t)
+    return Plan(n_ranks, threshold, bucket, [int(x) for x in numels],
+                [int(x) for x in submodule_of], persistent, offset, psi_p, psi_pad, S,
+                pers, buckets, segments, subs)
+
+
+# --------------------------------------------------------------------------
+# scalar preparation and elementwise arithmetic
+# --------------------------------------------------------------------------
+def bf16_rne(x: np.ndarray) -> np.ndarray:
+    """binary32 -> bfloat16 bit pattern, round to nearest, ties to even.
+
+    The fp32 master weights are written back to the 2-byte parameter
+    (ZeRO-1/2/3 concept page, compassingai.com, section 三階段機制詳解 /
+    Stage 1: fp32 master "截斷為 fp16" and written to the local half-precision
+    slice).  The pages' half type here is bf16 ("ddp-to-zero-memory-sharding",
+    section "先把账对齐"); "截斷" is read as "narrowing", rounded to nearest
+    even.  NaN inputs give a quiet NaN of the same sign.
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    with np.errstate(over="ignore"):
+        r = ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+    nan = (u & np.uint32(0x7FFFFFFF)) > np.uint32(0x7F800000)
+    if nan.any():
+        r[nan] = ((u[nan] >> np.uint32(16)) | np.uint32(0x40)).astype(np.uint16)
+    return r
+
+
+def bf16_to_f32(h: np.ndarray) -> np.ndarray:
+    """bfloat16 bit pattern -> binary32 (exact)."""
+    return (np.asarray(h, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _pow_by_mult(beta: float, t: int) -> float:
+    r = 1.0
+    for _ in range(t):
+        r *= beta
+    return r
+
+
+def adamw_scalars(hp: dict, t: int, n_ranks: int) -> Dict[str, np.float32]:
+    """Per-step binary32 scalars, derived once in float64 and rounded once.
+
+    AdamW (Loshchilov & Hutter, decoupled weight decay) with Kingma & Ba bias
+    correction; the hyper-parameter names are those of the ZERO tutorial's
+    example config (section 3.1: lr, betas, eps, weight_decay).  The pages
+    give no formula; this reading fixes one:
+        bc1 = 1 - beta1**t, bc2 = 1 - beta2**t (powers by repeated products)
+        step_size = lr / bc1, inv_sqrt_bc2 = 1 / sqrt(bc2),
+        decay = 1 - lr * weight_decay, inv_nd = 1 / N_d.
+    """
+    if t < 1:
+        raise ValueError("t is 1-based")
+    lr, b1, b2 = hp["lr"], hp["beta1"], hp["beta2"]
+    bc1 = 1.0 - _pow_by_mult(b1, t)
+    bc2 = 1.0 - _pow_by_mult(b2, t)
+    return dict(
+        step_size=F32(lr / bc1),
+        inv_sqrt_bc2=F32(1.0 / math.sqrt(bc2)),
+        decay=F32(1.0 - lr * hp["weight_decay"]),
+        b1=F32(b1), omb1=F32(1.0 - b1),
+        b2=F32(b2), omb2=F32(1.0 - b2),
+        eps=F32(hp["eps"]),
+        inv_nd=F32(1.0 / n_ranks),
+    )
+
+
+def reduce_sum(slices: Sequence[np.ndarray], inv_nd: np.float32) -> np.ndarray:
+    """Reduce the ranks' bf16 gradient slices into one fp32 slice.
+
+    Sum in rank order 0..N_d-1 with an fp32 accumulator, then scale by
+    f32(1/N_d).  The pages' reduce-scatter sums; the averaging is done
+    "elsewhere" ("ddp-to-zero-memory-sharding", section
+    "ZeRO-2：梯度为什么也可以分片", worked example G0=[2,6], G1=[4,10] ->
+    [3],[8]); here the scale is a multiply by the rounded reciprocal.
+    """
+    s = np.zeros(np.asarray(slices[0]).shape, dtype=np.float32)
+    for sl in slices:
+        s = s + bf16_to_f32(sl)
+    return s * inv_nd
+
+
+def adamw_update(g: np.ndarray, p: np.ndarray, m: np.ndarray, v: np.ndarray,
+                 sc: Dict[str, np.float32]):
+    """One AdamW update of fp32 master p and moments m, v from fp32 gradient g.
+
+    Elementwise and independent across elements, which is what lets each rank
+    update only its own slice ("ddp-to-zero-memory-sharding", section
+    "ZeRO-1：Optimizer States 为什么可以分片"; ZeRO-1/2/3 concept page,
+    Stage 1 mechanism).  Fixed operation order (each line one binary32 op
+    per element, no FMA):
+        p = p * decay
+        m = b1*m + omb1*g
+        v = b2*v + omb2*(g*g)
+        d = sqrt(v)*inv_sqrt_bc2 + eps
+        p = p - step_size*(m/d)
+    Returns new (p, m, v) arrays.
+    """
+    p = p * sc["decay"]
+    m = (sc["b1"] * m) + (sc["omb1"] * g)
+    v = (sc["b2"] * v) + (sc["omb2"] * (g * g))
+    d = (np.sqrt(v) * sc["inv_sqrt_bc2"]) + sc["eps"]
+    p = p - (sc["step_size"] * (m / d))
+    return p.astype(np.float32), m.astype(np.float32), v.astype(np.float32)
+
+
+# --------------------------------------------------------------------------
+# state containers
+# --------------------------------------------------------------------------
+@dataclass
+class ShardState:
+    """Per-rank optimizer state and bf16 shard (lists indexed by rank)."""
+    master: List[np.ndarray]
+    m: List[np.ndarray]
+    v: List[np.ndarray]
+    sparam: List[np.ndarray]
+
+
+@dataclass
+class PersistState:
+    master: np.ndarray
+    m: np.ndarray
+    v: np.ndarray
+    param: np.ndarray
+
+
+def init_state(plan: Plan, master_flat: np.ndarray, master_persist: np.ndarray):
+    """Initial state: given fp32 masters, m = v = 0, params = bf16(master).
+
+    master_flat has psi_pad elements; entries in [psi_p, psi_pad) are padding
+    and must be zero.  Returns (ShardState, full bf16 buffer, PersistState).
+    """
+    S = plan.shard_len
+    mf = np.asarray(master_flat, dtype=np.float32)
+    assert mf.shape == (plan.psi_pad,)
+    assert not mf[plan.psi_p:].any(), "padding must start at zero"
+    master = [mf[r * S:(r + 1) * S].copy() for r in range(plan.n_ranks)]
+    st = ShardState(master,
+                    [np.zeros(S, np.float32) for _ in range(plan.n_ranks)],
+                    [np.zeros(S, np.float32) for _ in range(plan.n_ranks)],
+                    [cast_bf16(x) for x in master])
+    full = allgather(plan, st.sparam)
+    mp = np.asarray(master_persist, dtype=np.float32).copy()
+    ps = PersistState(mp, np.zeros_like(mp), np.zeros_like(mp), cast_bf16(mp))
+    return st, full, ps
+
+
+def cast_bf16(master: np.ndarray) -> np.ndarray:
+    """fp32 master -> bf16 parameter slice (see bf16_rne)."""
+    return bf16_rne(master)
+
+
+# --------------------------------------------------------------------------
+# the sharded step, stage by stage
+# --------------------------------------------------------------------------
+def _rank_range(plan: Plan, r: int, flat_lo: int, flat_hi: int) -> Tuple[int, int]:
+    S = plan.shard_len
+    lo = max(flat_lo, r * S)
+    hi = min(flat_hi, (r + 1) * S)
+    if hi <= lo:
+        return 0, 0
+    return lo - r * S, hi - r * S
+
+
+def reduce_scatter(plan: Plan, grads: Sequence[np.ndarray], inv_nd: np.float32,
+                   flat_lo: int = 0, flat_hi: Optional[int] = None) -> List[Optional[np.ndarray]]:
+    """Gradient reduce-scatter: rank r receives the reduced slice
+    [r*S, (r+1)*S) of the flat gradient, restricted to [flat_lo, flat_hi).
+
+    grads[q] is rank q's local bf16 gradient of the flat partitioned buffer
+    (index f at grads[q][f]).  Follows "ddp-to-zero-memory-sharding",
+    section "ZeRO-2：梯度为什么也可以分片" (each GPU keeps only its slice of
+    the reduced gradient) and the ZeRO-1/2/3 concept page, Stage 3 mechanism
+    (ReduceScatter: each card keeps 1/N_d of the aggregated gradient).
+    Returns per rank the fp32 reduced slice of its local range (None if empty).
+    """
+    S = plan.shard_len
+    if flat_hi is None:
+        flat_hi = plan.psi_pad
+    out: List[Optional[np.ndarray]] = []
+    for r in range(plan.n_ranks):
+        a, b = _rank_range(plan, r, flat_lo, flat_hi)
+        if b <= a:
+            out.append(None)
+            continue
+        out.append(reduce_sum([np.asarray(G)[r * S + a:r * S + b] for G in grads], inv_nd))
+    return out
+
+
+def allgather(plan: Plan, sparam: Sequence[np.ndarray]) -> np.ndarray:
+    """Parameter all-gather: the full flat bf16 buffer is the ranks' shards
+    concatenated in rank order ("ddp-to-zero-memory-sharding", section
+    "ZeRO-1：Optimizer States 为什么可以分片": shards [9] and [18] gather to
+    [9, 18]; ZeRO-1/2/3 concept page, Stage 1 mechanism, AllGather)."""
+    return np.concatenate([np.asarray(s, dtype=np.uint16) for s in sparam]) \
+        if plan.n_ranks else np.zeros(0, np.uint16)
+
+
+def sharded_step(plan: Plan, hp: dict, t: int, grads: Sequence[np.ndarray],
+                 st: ShardState, full: np.ndarray,
+                 flat_lo: int = 0, flat_hi: Optional[int] = None) -> None:
+    """One ZeRO-3 optimizer step over flat range [flat_lo, flat_hi), in place.
+
+    The pages' per-step flow (encyclopedia entry "DeepSpeed ZeRO-3",
+    baike.kuaisou.com, section 原理 flowchart E->F: reduce-scatter gradient
+    shards, each process updates the optimizer state of its own shard; ZeRO
+    concept page, Stage 1/3 mechanism: update the fp32 slice, write it back to
+    the half-precision slice, all-gather):
+      1. reduce-scatter the bf16 local gradients (reduce_scatter)
+      2. AdamW on rank r's fp32 master/m/v slice (adamw_update)
+      3. cast the updated master to bf16 into the rank's shard (cast_bf16)
+      4. all-gather: write the rank's shard into the full buffer at r*S.
+    """
+    S = plan.shard_len
+    if flat_hi is None:
+        flat_hi = plan.psi_pad
+    sc = adamw_scalars(hp, t, plan.n_ranks)
+    gshard = reduce_scatter(plan, grads, sc["inv_nd"], flat_lo, flat_hi)
+    for r in range(plan.n_ranks):
+        g = gshard[r]
+        if g is None:
+            continue
+        a, b = _rank_range(plan, r, flat_lo, flat_hi)
+        p, m, v = adamw_update(g, st.master[r][a:b], st.m[r][a:b], st.v[r][a:b], sc)
+        st.master[r][a:b], st.m[r][a:b], st.v[r][a:b] = p, m, v
+        st.sparam[r][a:b] = cast_bf16(p)
+    gathered = allgather(plan, st.sparam)
+    lo, hi = flat_lo, flat_hi
+    full[lo:hi] = gathered[lo:hi]
+
+
+def persistent_step(plan: Plan, hp: dict, t: int, pgrads: Sequence[np.ndarray],
+                    ps: PersistState, replicas: Optional[int] = None) -> None:
+    """Update of the unpartitioned (persistent) group, in place.
+
+    Persistent parameters are neither partitioned nor released and stay
+    resident on every rank ("DeepSpeed Zero-3 的参数分区与按需访问机制",
+    小参数驻留).  Reading taken: their gradients are all-reduced (same fixed
+    order sum times 1/N_d) and every rank runs the full AdamW on its own copy.
+    The N_d replicas are computed separately here and checked to be bitwise
+    identical, then one copy is kept.
+    """
+    n = plan.n_ranks if replicas is None else replicas
+    sc = adamw_scalars(hp, t, plan.n_ranks)
+    g = reduce_sum(pgrads, sc["inv_nd"])
+    outs = [adamw_update(g, ps.master.copy(), ps.m.copy(), ps.v.copy(), sc) for _ in range(n)]
+    for o in outs[1:]:
+        for a, b in zip(o, outs[0]):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    ps.master[:], ps.m[:], ps.v[:] = outs[0]
+    ps.param[:] = cast_bf16(ps.master)
+
+
+# --------------------------------------------------------------------------
+# the unsharded data-parallel reference
+# --------------------------------------------------------------------------
+@dataclass
+class DDPState:
+    master: List[np.ndarray]     # one full copy per replica
+    m: List[np.ndarray]
+    v: List[np.ndarray]
+    param: List[np.ndarray]
+
+
+def ddp_init(plan: Plan, master_flat: np.ndarray) -> DDPState:
+    mf = np.asarray(master_flat, np.float32)
+    n = plan.n_ranks
+    return DDPState([mf.copy() for _ in range(n)],
+                    [np.zeros_like(mf) for _ in range(n)],
+                    [np.zeros_like(mf) for _ in range(n)],
+                    [cast_bf16(mf) for _ in range(n)])
+
+
+def ddp_step(plan: Plan, hp: dict, t: int, grads: Sequence[np.ndarray], st: DDPState) -> None:
+    """Standard data parallelism: all-reduce the gradients (every replica gets
+    the whole averaged gradient), then every replica runs the full AdamW on
+    its own full copy ("ddp-to-zero-memory-sharding", section
+    "DDP：每张 GPU 都在做一样的事", steps 4-5).  The replicas are kept
+    separately and must stay bitwise identical."""
+    sc = adamw_scalars(hp, t, plan.n_ranks)
+    gbar = reduce_sum([np.asarray(G)[:plan.psi_pad] for G in grads], sc["inv_nd"])
+    for d in range(plan.n_ranks):
+        p, m, v = adamw_update(gbar, st.master[d], st.m[d], st.v[d], sc)
+        st.master[d], st.m[d], st.v[d] = p, m, v
+        st.param[d] = cast_bf16(p)
+    for d in range(1, plan.n_ranks):
+        assert np.array_equal(st.master[d].view(np.uint32), st.master[0].view(np.uint32))
+
+
+# --------------------------------------------------------------------------
+# fetch / release of a submodule (parameter state machine)
+# --------------------------------------------------------------------------
+def fetch_submodule(plan: Plan, k: int, sparam: Sequence[np.ndarray],
+                    persist_param: np.ndarray) -> np.ndarray:
+    """Gather submodule k's parameters into one contiguous bf16 tensor.
+
+    Before a submodule's forward (and again before its backward) its
+    parameter shards are all-gathered into full tensors, and the non-local
+    part is released after use (encyclopedia entry, section 原理; ZeRO
+    concept page, "ZeRO Stage 3 的 AllGather 與釋放機制").  Layout: the
+    member tensors in list order, each element f of a partitioned tensor read
+    from rank f // S at local index f % S, persistent tensors read from the
+    resident persistent copy.
+    """
+    S = plan.shard_len
+    parts = []
+    for t in plan.submodules.get(k, []):
+        n = plan.numel[t]
+        if plan.persistent[t]:
+            o = plan.offset[t]
+            parts.append(np.asarray(persist_param[o:o + n], np.uint16))
+        else:
+            f = np.arange(plan.offset[t], plan.offset[t] + n, dtype=np.int64)
+            out = np.empty(n, np.uint16)
+            for r in range(plan.n_ranks):
+                sel = (f // S) == r
+                if sel.any():
+                    out[sel] = np.asarray(sparam[r])[f[sel] - r * S]
+            parts.append(out)
+    return np.concatenate(parts) if parts else np.zeros(0, np.uint16)
+
+
+class SubmoduleStates:
+    """NOT_AVAILABLE -> (gather issued) INFLIGHT -> (done) AVAILABLE
+    -> (reference count back to zero) NOT_AVAILABLE
+    ("DeepSpeed Zero-3 的参数分区与按需访问机制", the ZeroParamStatus state
+    machine).  A second fetch of a fetched submodule only adds a reference;
+    releasing a NOT_AVAILABLE submodule is an error."""
+
+    def __init__(self, n: int):
+        self.status = [NOT_AVAILABLE] * n
+        self.refs = [0] * n
+
+    def fetch(self, k: int) -> bool:
+        """Returns True when a gather must be issued."""
+        if self.status[k] == NOT_AVAILABLE:
+            self.status[k] = INFLIGHT
+            self.refs[k] = 1
+            return True
+        self.refs[k] += 1
+        return False
+
+    def complete(self, k: int) -> None:
+        if self.status[k] == INFLIGHT:
+            self.status[k] = AVAILABLE
+
+    def release(self, k: int) -> None:
+        if self.status[k] == NOT_AVAILABLE:
+            raise RuntimeError("release of a submodule that is not fetched")
+        self.refs[k] -= 1
+        if self.refs[k] == 0:
+            self.status[k] = NOT_AVAILABLE
+
+
+# --------------------------------------------------------------------------
+# accounting
+# --------------------------------------------------------------------------
+def memory_bytes(stage: int, psi: float, n_d: int, K: int = 12) -> float:
+    """Model-state bytes per rank, mixed precision with 2-byte params and
+    grads and K bytes of optimizer state per parameter (K = 12 for Adam).
+
+    stage 0 (plain DP): (2+2+K)Ψ; stage 1: 2Ψ+2Ψ+KΨ/N_d;
+    stage 2: 2Ψ+(2+K)Ψ/N_d; stage 3: (2+2+K)Ψ/N_d
+    (encyclopedia entry, section 原理; ZeRO concept page, section
+    三階段記憶體公式彙總; "ddp-to-zero-memory-sharding", sections
+    "ZeRO-1..3" and "28 GB 是怎么来的").
+    """
+    if stage == 0:
+        return (2 + 2 + K) * psi
+    if stage == 1:
+        return 2 * psi + 2 * psi + K * psi / n_d
+    if stage == 2:
+        return 2 * psi + (2 + K) * psi / n_d
+    if stage == 3:
+        return (2 + 2 + K) * psi / n_d
+    raise ValueError("stage must be 0..3")
+
+
+def comm_elems(stage: int, psi: float) -> float:
+    """Elements communicated per rank per step before the ring factor:
+    all-reduce = reduce-scatter + all-gather = 2Ψ for plain DP and stages
+    1-2; stage 3 adds a second parameter all-gather (forward and backward):
+    3Ψ (ZeRO concept page, "通訊量對比 (Stage 3 vs 基線 DP)")."""
+    if stage in (0, 1, 2):
+        return 2.0 * psi
+    if stage == 3:
+        return 3.0 * psi
+    raise ValueError("stage must be 0..3")
+
+
+def ring_send_bytes(stage: int, psi: float, n_d: int, elem_bytes: int = 2) -> float:
+    """Per-GPU bytes sent by ring collectives: each collective over a tensor
+    of size X sends (N-1)/N * X per GPU ("ddp-to-zero-memory-sharding",
+    section "为什么 ZeRO-2 的通信量和 DDP 接近", V = (N-1)/N * S)."""
+    return comm_elems(stage, psi) * elem_bytes * (n_d - 1) / n_d

@@ -1,0 +1,413 @@
+"""Benchmark of the ZeRO-3 hot path: one step = a forward and a backward
+gather of every submodule plus the fused reduce-scatter/AdamW/cast/all-gather
+step over every virtual rank and the persistent group.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decoder_1p3b|gpt2_small|llama_7b_rank0]
+
+Prints one JSON line (rank 0).  N > 1 runs one replica of the workload per
+GPU (the emulated ranks live inside each GPU; there is no inter-GPU step),
+launched by torch.distributed.run; value is the params of all replicas per
+second (weak scaling).  --impl reference times the CPU oracle on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused ZeRO-3 step params/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+PROFILE = os.path.join(ROOT, "profiles", "zero3_step_fused_decoder_1p3b.md")
+
+WORKLOADS = {
+    # name: (factory, state ranks, bucketed, description)
+    "decoder_1p3b": ("decoder_1p3b", None, False,
+                     "1.3B GPT-style decoder (24L, d=2048, vocab 50257), N_d=8 virtual ranks, "
+                     "full emulation in one HBM"),
+    "gpt2_small": ("gpt2_small", None, False,
+                   "GPT-2-small list (12L, d=768, vocab 50257), N_d=4 virtual ranks"),
+    "llama_7b_rank0": ("llama_7b_rank0", [0], True,
+                       "Llama-7B list (32L, d=4096, SwiGLU 11008, vocab 32000), rank-0 view at "
+                       "N_d=8: rank 0's state resident, gradients per 5e8-element bucket"),
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decoder_1p3b")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profile_traffic(kernels_sha: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu
+    summary, if it was captured on the current kernel source."""
+    if not os.path.exists(PROFILE):
+        return None
+    txt = open(PROFILE).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(kernels\.cu sha256 ([0-9a-f]+)\)", txt)
+    if not m or m.group(2) != kernels_sha:
+        return None
+    return float(m.group(1))
+
+
+def kernels_sha() -> str:
+    p = os.path.join(ROOT, "zero_sharded_optimizer_shard_gb300", "csrc", "kernels.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm, smax, pw = [], [], []
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                pw.append(float(r[3]))
+            except ValueError:
+                continue
+            for k, name in enumerate(names):
+                if r[5 + k].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_oracle_rate(wname: str, budget_s: float = 15.0):
+    """The CPU oracle, as it stands, on a bounded contiguous sample of rank
+    0's shard: all N_d ranks' gradients for the sample, the reduce, AdamW and
+    bf16 cast.  Returns (params/s, description)."""
+    import numpy as np
+
+    import oracle as O
+    from zero_sharded_optimizer_shard_gb300 import synth, workloads as W
+
+    w = getattr(W, WORKLOADS[wname][0])() if wname != "llama_7b_rank0" else W.llama_7b()
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    rng_n = 1 << 20
+    idx = np.arange(rng_n, dtype=np.int64)
+    grads = [synth.normal_bf16(w.seed, W.STREAM_GRAD, 1, q, idx, w.grad_sigma, w.outlier_p,
+                               w.outlier_sigma) for q in range(plan.n_ranks)]
+    p = synth.normal_f32(w.seed, W.STREAM_MASTER, 0, 0, idx, w.master_sigma)
+    m = np.zeros_like(p)
+    v = np.zeros_like(p)
+
+    def one(t, p, m, v):
+        sc = O.adamw_scalars(w.hparams, t, plan.n_ranks)
+        g = O.reduce_sum(grads, sc["inv_nd"])
+        p, m, v = O.adamw_update(g, p, m, v, sc)
+        return p, m, v, O.cast_bf16(p)
+
+    t0 = time.perf_counter()
+    p, m, v, _ = one(1, p, m, v)
+    dt1 = time.perf_counter() - t0
+    reps = max(1, int(budget_s / max(dt1, 1e-3)))
+    t0 = time.perf_counter()
+    for t in range(2, 2 + reps):
+        p, m, v, _ = one(t, p, m, v)
+    dt = time.perf_counter() - t0
+    rate = rng_n * reps / dt
+    return rate, (f"{rng_n} consecutive elements of rank 0's shard, all {plan.n_ranks} ranks' "
+                  f"gradients, {reps} steps (numpy, one thread)"), dt
+
+
+def run_reference(args):
+    import numpy as np  # noqa: F401
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    budget = 4.0
+    rates = []
+    desc = None
+    for i in range(args.warmup + args.steps):
+        r, desc, _ = cpu_oracle_rate(args.workload, budget_s=budget)
+        if i >= args.warmup:
+            rates.append(r)
+    value = sum(rates) / len(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.workload][3]},
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def launches_per_step(e) -> int:
+    """Kernel launches of one full step, counted from the plan: the fused
+    kernel once per gradient chunk, the persistent group once, and each
+    submodule gather ceil(pieces / 64) times, twice (forward, backward)."""
+    import math
+    n = 0
+    for k in range(e.plan.info.n_submodules):
+        pieces = 0
+        for t, sub in enumerate(e.w.submodule_of):
+            if sub != k or e.w.numels[t] == 0:
+                continue
+            ti = e.plan.tensor(t)
+            pieces += 1 if ti.persistent else ti.n_segments
+        n += 2 * math.ceil(pieces / 64)
+    return n + len(e.chunks) + (1 if e.psi_s > 0 else 0)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from zero_sharded_optimizer_shard_gb300 import build as b
+    if rank == 0 or world == 1:
+        b.build_all(quiet=True)
+    if world > 1:
+        dist.barrier()
+    from zero_sharded_optimizer_shard_gb300 import workloads as W, zero3
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+
+    fac, state_ranks, bucketed, desc = WORKLOADS[args.workload]
+    w = getattr(W, fac)() if fac != "llama_7b_rank0" else W.llama_7b()
+    stream = torch.cuda.Stream()
+    e = Emulation(w, device=f"cuda:{local}", state_ranks=state_ranks, bucketed=bucketed,
+                  stream=stream)
+    with torch.cuda.stream(stream):
+        e.init_params()
+        e.fill_grads(1)   # generated once before timing, reused by every step
+    torch.cuda.synchronize()
+    nbytes = e.step_bytes()
+    n_params = w.psi if state_ranks is None else nbytes["flat_elems"] + e.psi_s
+
+    def full_step(t, ev_a=None, ev_b=None):
+        e.forward_backward_gathers()
+        if ev_a is not None:
+            ev_a.record(stream)
+        for (a_, b_), G in zip(e.chunks, e.grads):
+            zero3.zero3_step(e.plan, e.hp, t, e.ptrs(G), a_, e.ptrs(e.master), e.ptrs(e.m),
+                             e.ptrs(e.v), e.ptrs(e.sparam), e.full.data_ptr(), None, a_, b_, e.sid)
+        if ev_b is not None:
+            ev_b.record(stream)
+        zero3.zero3_persistent_step(e.plan, e.hp, t, e.persist, e.sid)
+
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        full_step(t)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    start.record(stream)
+    for k in range(args.steps):
+        t += 1
+        full_step(t, *evs[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    ms = start.elapsed_time(end)
+    fused_ms = [a.elapsed_time(b) for a, b in evs]
+    clk = clocks.stop()
+    if world > 1:
+        x = torch.tensor([ms], device=f"cuda:{local}", dtype=torch.float64)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        ms = float(x.item())
+
+    # ---- end to end through the public API: host gradients in, params out
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(e, w, args, stream, n_params, t)
+        if world > 1 and e2e is not None:
+            x = torch.tensor([e2e["ms_per_step"]], device=f"cuda:{local}", dtype=torch.float64)
+            dist.all_reduce(x, op=dist.ReduceOp.MAX)
+            e2e["value"] = world * n_params / (float(x.item()) / 1e3)
+            e2e["ms_per_step"] = float(x.item())
+
+    if rank == 0:
+        ms_step = ms / args.steps
+        fused_launch_ms = statistics.mean(fused_ms) / max(len(e.chunks), 1)
+        fused_bytes_launch = nbytes["fused"] / max(len(e.chunks), 1)
+        peak, peak_kind = peaks()
+        achieved = fused_bytes_launch / (fused_launch_ms / 1e3) / 1e9
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            rate, sample, _ = cpu_oracle_rate(args.workload, budget_s=15.0)
+            cpu = {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
+                   "sample": sample}
+        step_gbs = nbytes["total"] / (ms_step / 1e3) / 1e9
+        line = {
+            "metric": METRIC,
+            "value": world * n_params / (ms_step / 1e3),
+            "unit": "params/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic",
+            "config": {
+                "workload": desc, "name": args.workload, "n_ranks": w.n_ranks,
+                "params": n_params, "psi_pad": e.psi_pad, "psi_s": e.psi_s,
+                "bytes_per_step": nbytes["total"],
+                "step": "forward + backward gather of every submodule, fused step, persistent group",
+                "l2": f"inputs larger than L2 ({nbytes['total'] / 1e9:.1f} GB touched per step)",
+                "grads": "generated once on the device before timing, reused by every step",
+                "parallelism": f"{world} replica(s) x {w.n_ranks} emulated ranks",
+            },
+            "step_gbs": step_gbs,
+            "step_hbm_frac": step_gbs / peak,
+            "fused_step": {"ms_per_launch": fused_launch_ms, "launches_per_step": len(e.chunks),
+                           "bytes_per_launch": fused_bytes_launch,
+                           "bytes_per_elem": 2 * w.n_ranks + 28,
+                           "params_per_s": nbytes["flat_elems"] / max(len(e.chunks), 1)
+                           / (fused_launch_ms / 1e3)},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": profile_traffic(kernels_sha()),
+                         "kernel": "stream_kernel<kFused, N_d> (zero3_step)"},
+            "gpu_launches": launches_per_step(e) * args.steps,
+            "clocks": clk,
+            "wall_s_timed": wall,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(e, w, args, stream, n_params, t0):
+    """Same step through the public API with host buffers: every step copies
+    every rank's local gradients (and the persistent-group gradients) from
+    pinned host memory, runs the step, and reads the full bf16 parameter
+    buffer back into pinned host memory."""
+    import torch
+    steps = max(1, min(args.steps, 5))
+    try:
+        host_g = [[torch.empty(x.numel(), dtype=x.dtype, pin_memory=True) for x in G] for G in e.grads]
+        host_pg = [torch.empty(x.numel(), dtype=x.dtype, pin_memory=True) for x in e.pgrads]
+        host_full = torch.empty(e.full.numel(), dtype=e.full.dtype, pin_memory=True)
+    except RuntimeError as exc:
+        return {"value": None, "unit": "params/s", "error": f"pinned host allocation failed: {exc}"}
+    for hG, G in zip(host_g, e.grads):
+        for h, d in zip(hG, G):
+            h.copy_(d)
+    for h, d in zip(host_pg, e.pgrads):
+        h.copy_(d)
+    h2d = sum(x.numel() * 2 for hG in host_g for x in hG) + sum(x.numel() * 2 for x in host_pg)
+    d2h = host_full.numel() * 2
+    torch.cuda.synchronize()
+    t = t0
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.perf_counter()
+    start.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            t += 1
+            for hG, G in zip(host_g, e.grads):
+                for h, d in zip(hG, G):
+                    d.copy_(h, non_blocking=True)
+            for h, d in zip(host_pg, e.pgrads):
+                d.copy_(h, non_blocking=True)
+            e.full_step(t)
+            host_full.copy_(e.full, non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    ms = start.elapsed_time(end) / steps
+    return {"value": n_params / (ms / 1e3), "unit": "params/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms,
+            "wall_ms_per_step": wall * 1e3 / steps}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

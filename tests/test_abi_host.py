@@ -1,0 +1,227 @@
+"""Host-side tests of the C ABI: exports, planner parity with the oracle,
+accounting, argument validation and the submodule state machine's host
+transitions.  No call here launches a kernel: every compute call below
+carries at least one invalid argument, which the library rejects before it
+touches the GPU."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+from zero_sharded_optimizer_shard_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "zero3.h")
+
+
+def header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(zero3_[a-z_]+)\s*\(", src)))
+
+
+def test_header_lists_every_binding_function():
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    assert header_functions() == sorted(zero3.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_synth_library_exports(lib):
+    from zero_sharded_optimizer_shard_gb300 import synth_device
+    assert hasattr(synth_device.load(), "zero3synth_normal")
+
+
+# ---------------------------------------------------------------- planner parity
+def _compare_plan(numels, subs, nd, thr, bucket):
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    ref = O.partition(numels, subs, nd, thr, bucket)
+    p = zero3.Plan(numels, subs, nd, thr, bucket)
+    i = p.info
+    assert (i.n_ranks, i.psi_p, i.psi_pad, i.shard_len, i.psi_s) == \
+        (nd, ref.psi_p, ref.psi_pad, ref.shard_len, ref.psi_s)
+    assert i.n_tensors == len(numels)
+    assert i.n_persistent == sum(ref.persistent)
+    assert i.n_buckets == len(ref.buckets)
+    assert [p.bucket(b) for b in range(i.n_buckets)] == ref.buckets
+    assert i.n_submodules == ref.n_submodules
+    for k in range(i.n_submodules):
+        assert p.submodule(k) == (len(ref.submodules.get(k, [])), ref.submodule_numel(k))
+    for t in range(len(numels)):
+        ti = p.tensor(t)
+        assert (ti.numel, ti.offset, bool(ti.persistent), ti.submodule) == \
+            (ref.numel[t], ref.offset[t], ref.persistent[t], ref.submodule[t])
+        segs = p.segments(t)
+        assert segs == ref.segments[t]
+        if segs:
+            assert (ti.first_rank, ti.last_rank) == (segs[0][0], segs[-1][0])
+        else:
+            assert (ti.first_rank, ti.last_rank) == (-1, -1)
+
+
+@pytest.mark.parametrize("name", ["toy_mlp", "gpt2_small", "decoder_1p3b", "llama_7b_rank0",
+                                  "ragged"])
+def test_planner_matches_oracle_on_workloads(lib, name):
+    w = W.BY_NAME[name]()
+    _compare_plan(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+
+
+def test_planner_matches_oracle_brute_force(lib):
+    rng = np.random.default_rng(7)
+    for trial in range(400):
+        nd = int(rng.integers(1, 10))
+        n_t = int(rng.integers(0, 9))
+        numels = [int(x) for x in rng.integers(0, 40, n_t)]
+        subs = [int(x) for x in rng.integers(0, 4, n_t)] if rng.random() < 0.5 else None
+        _compare_plan(numels, subs, nd, int(rng.integers(0, 20)), int(rng.integers(1, 30)))
+
+
+def test_planner_large_rank_counts(lib):
+    _compare_plan([10**6 + 3, 5, 77777, 2 * 10**5], None, 64, 100_000, 10**5)
+    _compare_plan([1], None, 64, 0, 1)
+
+
+# ---------------------------------------------------------------- accounting
+def test_accounting_matches_oracle(lib):
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    for stage in range(4):
+        for psi, nd in [(7e9, 4), (7.5e9, 64), (1.3e9, 8), (1.0, 1)]:
+            assert zero3.zero3_memory_bytes(stage, psi, nd) == pytest.approx(
+                O.memory_bytes(stage, psi, nd), rel=1e-15)
+            assert 2 * zero3.zero3_comm_elems(stage, psi, nd) == pytest.approx(
+                O.ring_send_bytes(stage, psi, nd), rel=1e-15)
+    # the pages' 7B / 4 GPU numbers through the library
+    assert zero3.zero3_memory_bytes(3, 7e9, 4) == 28e9
+    assert 2 * zero3.zero3_comm_elems(3, 7e9, 4) == pytest.approx(31.5e9)
+
+
+def test_accounting_rejects_bad_arguments(lib):
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    out = C.c_double()
+    assert zero3.raw_status("zero3_memory_bytes", 4, 1.0, 4, C.byref(out)) == zero3.EINVAL
+    assert zero3.raw_status("zero3_memory_bytes", 3, 1.0, 0, C.byref(out)) == zero3.EINVAL
+    assert zero3.raw_status("zero3_comm_elems", -1, 1.0, 4, C.byref(out)) == zero3.EINVAL
+    assert zero3.raw_status("zero3_comm_elems", 3, 1.0, 4, None) == zero3.EINVAL
+
+
+# ---------------------------------------------------------------- validation
+def test_partition_rejects_bad_arguments(lib):
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    out = C.c_void_p()
+    n = (C.c_int64 * 2)(10, 20)
+    neg = (C.c_int64 * 2)(10, -1)
+    bad_sub = (C.c_int32 * 2)(0, -3)
+    for args in [(n, None, 2, 0, 0, 1), (n, None, 2, 65, 0, 1), (neg, None, 2, 2, 0, 1),
+                 (n, None, 2, 2, -1, 1), (n, None, 2, 2, 0, 0), (n, bad_sub, 2, 2, 0, 1),
+                 (None, None, 2, 2, 0, 1), (n, None, -1, 2, 0, 1)]:
+        assert zero3.raw_status("zero3_partition", *args, C.byref(out)) == zero3.EINVAL, args
+    assert zero3.raw_status("zero3_partition", n, None, 2, 2, 0, 1, None) == zero3.EINVAL
+
+
+FAKE = 1 << 20       # a 16-byte aligned fake device address (never dereferenced)
+MISALIGNED = FAKE + 2
+
+
+def _plan(nd=2):
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    return zero3.Plan([1000, 10, 2000], [0, 0, 1], nd, threshold=100, bucket=512)
+
+
+def test_step_rejects_bad_arguments_before_any_launch(lib):
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    p = _plan()
+    hp = zero3.hparams()
+    lo, hi = 0, p.info.psi_pad
+    ok = [FAKE, FAKE]
+    P = zero3._ptrs
+
+    def step(t=1, grads=ok, origin=0, master=ok, m=ok, v=ok, sparam=ok, full=FAKE, lo=lo, hi=hi,
+             hp_=hp):
+        return zero3.raw_status("zero3_step", p.handle, C.byref(hp_) if hp_ is not None else None,
+                                t, P(grads), origin, P(master), P(m), P(v), P(sparam), full,
+                                None, lo, hi, None)
+
+    E = zero3.EINVAL
+    assert step(t=0) == E
+    assert step(hp_=None) == E
+    assert step(hp_=zero3.hparams(beta1=1.0)) == E
+    assert step(hp_=zero3.hparams(lr=float("nan"))) == E
+    assert step(hi=hi + 1) == E
+    assert step(lo=5, hi=4) == E
+    assert step(origin=1) == E
+    assert step(grads=[FAKE, 0]) == E                  # a missing rank
+    assert step(grads=[FAKE, MISALIGNED]) == E
+    assert step(grads=None) == E
+    assert step(master=[FAKE, 0]) == E
+    assert step(v=[MISALIGNED, FAKE]) == E
+    assert step(sparam=[FAKE, MISALIGNED]) == E
+    assert step(full=0) == E
+    assert step(full=MISALIGNED) == E
+    # a rank outside the range may pass NULL state, but the range here covers
+    # both ranks
+    assert step(lo=0, hi=p.info.shard_len, master=[FAKE, 0], full=MISALIGNED) == E
+    # the persistent group is validated before the main launch
+    ps = zero3.persist_state([FAKE, 0], FAKE, FAKE, FAKE, FAKE)
+    st = zero3.raw_status("zero3_step", p.handle, C.byref(hp), 1, P(ok), 0, P(ok), P(ok), P(ok),
+                          P(ok), FAKE, C.byref(ps), lo, hi, None)
+    assert st == E
+
+
+def test_unfused_calls_reject_bad_arguments(lib):
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    p = _plan(3)
+    hp = zero3.hparams()
+    ok = [FAKE] * 3
+    P = zero3._ptrs
+    hi = p.info.psi_pad
+    E = zero3.EINVAL
+    assert zero3.raw_status("zero3_reduce_scatter", p.handle, P(ok), 0, 0, hi, P(ok), 7,
+                            None) == E
+    assert zero3.raw_status("zero3_reduce_scatter", p.handle, P([FAKE, FAKE, 0]), 0, 0, hi, P(ok),
+                            zero3.F32, None) == E
+    assert zero3.raw_status("zero3_adamw_step", p.handle, C.byref(hp), 1, P(ok), zero3.F32,
+                            P(ok), P(ok), P(ok), P([FAKE, MISALIGNED, FAKE]), 0, hi, None) == E
+    assert zero3.raw_status("zero3_allgather", p.handle, P(ok), MISALIGNED, 0, hi, None) == E
+    assert zero3.raw_status("zero3_cast_params", p.handle, P(ok), P(ok), MISALIGNED, None, 0, hi,
+                            None) == E
+    # empty ranges are no-ops and need no pointers
+    assert zero3.raw_status("zero3_allgather", p.handle, None, 0, 3, 3, None) == zero3.OK
+    assert zero3.raw_status("zero3_reduce_scatter", p.handle, None, 0, 0, 0, None, zero3.F32,
+                            None) == zero3.OK
+
+
+def test_submodule_state_errors_on_host(lib):
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    p = _plan()
+    assert zero3.zero3_submodule_status(p, 0) == zero3.NOT_AVAILABLE
+    with pytest.raises(zero3.Zero3Error) as e:
+        zero3.zero3_release_submodule(p, 0)
+    assert e.value.status == zero3.ESTATE
+    with pytest.raises(zero3.Zero3Error) as e:
+        zero3.zero3_submodule_wait(p, 1)
+    assert e.value.status == zero3.ESTATE
+    for bad in (-1, 2):
+        with pytest.raises(zero3.Zero3Error) as e:
+            zero3.zero3_submodule_status(p, bad)
+        assert e.value.status == zero3.EINVAL
+    # misaligned output or a missing owner shard is rejected before any work
+    st = zero3.raw_status("zero3_fetch_submodule", p.handle, 0, zero3._ptrs([FAKE, FAKE]), FAKE,
+                          MISALIGNED, None)
+    assert st == zero3.EINVAL
+    st = zero3.raw_status("zero3_fetch_submodule", p.handle, 1, zero3._ptrs([FAKE, 0]), FAKE,
+                          FAKE, None)
+    assert st == zero3.EINVAL
+    assert zero3.zero3_submodule_status(p, 0) == zero3.NOT_AVAILABLE
+
+
+def test_status_strings(lib):
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    assert zero3.status_string(zero3.OK) == "ok"
+    assert "invalid" in zero3.status_string(zero3.EINVAL)
+    assert zero3.status_string(99) == "unknown status"

@@ -1,0 +1,413 @@
+// C ABI of the compute calls: argument checks, the per-rank spans of a flat
+// range, the submodule state machine, and the launches.
+#include <cmath>
+#include <cstring>
+
+#include "internal.h"
+
+namespace {
+
+using z3::Span;
+using z3::StreamArgs;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool range_ok(const zero3_plan* p, int64_t lo, int64_t hi) {
+    return 0 <= lo && lo <= hi && hi <= p->psi_pad;
+}
+
+bool hparams_ok(const zero3_adamw_hparams* hp, int64_t t) {
+    if (!hp || t < 1) return false;
+    const double v[5] = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
+    for (double x : v)
+        if (!std::isfinite(x)) return false;
+    return hp->beta1 >= 0.0 && hp->beta1 < 1.0 && hp->beta2 >= 0.0 && hp->beta2 < 1.0 &&
+           hp->lr >= 0.0 && hp->eps >= 0.0;
+}
+
+zero3_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ZERO3_OK : ZERO3_ECUDA; }
+
+// Checks the N_d gradient pointers: present and 16-byte aligned.
+bool grads_ok(const zero3_plan* p, const uint16_t* const* grads) {
+    if (!grads) return false;
+    for (int q = 0; q < p->n_ranks; ++q)
+        if (!grads[q] || !aligned16(grads[q])) return false;
+    return true;
+}
+
+// Local range of rank r inside flat [lo, hi); empty when b <= a.
+void rank_range(const zero3_plan* p, int r, int64_t lo, int64_t hi, int64_t* a, int64_t* b) {
+    const int64_t s0 = static_cast<int64_t>(r) * p->S, s1 = s0 + p->S;
+    *a = (lo > s0 ? lo : s0) - s0;
+    *b = (hi < s1 ? hi : s1) - s0;
+}
+
+// Appends a span and advances the chunk counter.
+void add_span(StreamArgs& a, Span s) {
+    const int64_t first = s.lo & ~static_cast<int64_t>(7);
+    s.chunk0 = a.total_chunks;
+    a.span[a.n_spans++] = s;
+    a.total_chunks += (s.hi - first + 7) / 8;
+}
+
+struct RankPtrs {
+    const uint16_t* const* grads = nullptr;
+    int64_t grads_origin = 0;
+    float* const* master = nullptr;
+    float* const* m = nullptr;
+    float* const* v = nullptr;
+    void* const* out = nullptr;        // sparam or shard grad
+    const void* const* in = nullptr;   // shard grad, sparam or master
+    int out_elem = 2;                  // bytes per element of out
+    int in_elem = 0;                   // bytes per element of in (0: unused)
+    uint16_t* full = nullptr;
+    bool need_state = false;
+};
+
+// Builds the launch description of one mode over flat [lo, hi).  Validates
+// the pointers of every rank that owns part of the range.
+zero3_status build_args(const zero3_plan* p, int mode, const RankPtrs& rp, int64_t lo, int64_t hi,
+                        const z3::Scalars* sc, int dtype, StreamArgs& a) {
+    std::memset(&a, 0, sizeof(a));
+    a.nd = p->n_ranks;
+    a.dtype = dtype;
+    a.full = rp.full;
+    if (sc) a.sc = *sc;
+    if (rp.grads)
+        for (int q = 0; q < p->n_ranks; ++q) a.grads[q] = rp.grads[q];
+    for (int r = 0; r < p->n_ranks; ++r) {
+        int64_t la, lb;
+        rank_range(p, r, lo, hi, &la, &lb);
+        if (lb <= la) continue;
+        Span s;
+        std::memset(&s, 0, sizeof(s));
+        s.lo = la;
+        s.hi = lb;
+        bool vec = true;
+        if (rp.grads) {
+            s.gofs = static_cast<int64_t>(r) * p->S - rp.grads_origin;
+            vec = vec && (s.gofs % 8 == 0);
+        }
+        if (rp.full) {
+            s.fofs = static_cast<int64_t>(r) * p->S;
+            vec = vec && (s.fofs % 8 == 0);
+        } else {
+            s.fofs = -1;
+        }
+        if (rp.need_state) {
+            if (!rp.master || !rp.m || !rp.v) return ZERO3_EINVAL;
+            s.master = rp.master[r];
+            s.m = rp.m[r];
+            s.v = rp.v[r];
+            if (!s.master || !s.m || !s.v) return ZERO3_EINVAL;
+            if (!aligned16(s.master) || !aligned16(s.m) || !aligned16(s.v)) return ZERO3_EINVAL;
+        }
+        if (rp.out) {
+            s.out = rp.out[r];
+            if (!s.out || !aligned16(s.out)) return ZERO3_EINVAL;
+        }
+        if (rp.in) {
+            s.in = rp.in[r];
+            if (!s.in || !aligned16(s.in)) return ZERO3_EINVAL;
+        }
+        s.vec = vec ? 1 : 0;
+        add_span(a, s);
+    }
+    return ZERO3_OK;
+}
+
+z3::Scalars step_scalars(const zero3_plan* p, const zero3_adamw_hparams* hp, int64_t t) {
+    return z3::make_scalars(*hp, t, p->n_ranks);
+}
+
+bool persist_ok(const zero3_plan* p, const zero3_persist_state* ps) {
+    if (p->psi_s == 0) return true;
+    return ps && grads_ok(p, ps->grads) && ps->master && ps->m && ps->v && ps->param &&
+           aligned16(ps->master) && aligned16(ps->m) && aligned16(ps->v) && aligned16(ps->param);
+}
+
+zero3_status persistent_launch(const zero3_plan* p, const z3::Scalars& sc,
+                               const zero3_persist_state* ps, cudaStream_t stream) {
+    if (p->psi_s == 0) return ZERO3_OK;
+    if (!persist_ok(p, ps)) return ZERO3_EINVAL;
+    StreamArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.nd = p->n_ranks;
+    a.sc = sc;
+    for (int q = 0; q < p->n_ranks; ++q) a.grads[q] = ps->grads[q];
+    Span s;
+    std::memset(&s, 0, sizeof(s));
+    s.lo = 0;
+    s.hi = p->psi_s;
+    s.gofs = 0;
+    s.fofs = -1;
+    s.master = ps->master;
+    s.m = ps->m;
+    s.v = ps->v;
+    s.out = ps->param;
+    s.vec = 1;
+    add_span(a, s);
+    return cuda_status(z3::launch_stream(z3::kFused, a, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+zero3_status zero3_reduce_scatter(const zero3_plan* p, const uint16_t* const* grads,
+                                  int64_t grads_origin, int64_t lo, int64_t hi,
+                                  void* const* shard_grad, zero3_dtype out_dtype,
+                                  zero3_stream stream) {
+    if (!p || !range_ok(p, lo, hi) || grads_origin > lo) return ZERO3_EINVAL;
+    if (out_dtype != ZERO3_BF16 && out_dtype != ZERO3_F32) return ZERO3_EINVAL;
+    if (lo == hi) return ZERO3_OK;
+    if (!grads_ok(p, grads) || !shard_grad) return ZERO3_EINVAL;
+    RankPtrs rp;
+    rp.grads = grads;
+    rp.grads_origin = grads_origin;
+    rp.out = shard_grad;
+    z3::Scalars sc;
+    std::memset(&sc, 0, sizeof(sc));
+    sc.inv_nd = static_cast<float>(1.0 / static_cast<double>(p->n_ranks));
+    StreamArgs a;
+    zero3_status st = build_args(p, z3::kReduce, rp, lo, hi, &sc, out_dtype, a);
+    if (st != ZERO3_OK) return st;
+    return cuda_status(z3::launch_stream(z3::kReduce, a, stream));
+}
+
+zero3_status zero3_adamw_step(const zero3_plan* p, const zero3_adamw_hparams* hp, int64_t t,
+                              const void* const* shard_grad, zero3_dtype grad_dtype,
+                              float* const* master, float* const* m, float* const* v,
+                              uint16_t* const* sparam, int64_t lo, int64_t hi,
+                              zero3_stream stream) {
+    if (!p || !range_ok(p, lo, hi) || !hparams_ok(hp, t)) return ZERO3_EINVAL;
+    if (grad_dtype != ZERO3_BF16 && grad_dtype != ZERO3_F32) return ZERO3_EINVAL;
+    if (lo == hi) return ZERO3_OK;
+    if (!shard_grad || !sparam) return ZERO3_EINVAL;
+    RankPtrs rp;
+    rp.master = master;
+    rp.m = m;
+    rp.v = v;
+    rp.need_state = true;
+    rp.out = reinterpret_cast<void* const*>(sparam);
+    rp.in = shard_grad;
+    const z3::Scalars sc = step_scalars(p, hp, t);
+    StreamArgs a;
+    zero3_status st = build_args(p, z3::kAdam, rp, lo, hi, &sc, grad_dtype, a);
+    if (st != ZERO3_OK) return st;
+    return cuda_status(z3::launch_stream(z3::kAdam, a, stream));
+}
+
+zero3_status zero3_allgather(const zero3_plan* p, const uint16_t* const* sparam, uint16_t* full,
+                             int64_t lo, int64_t hi, zero3_stream stream) {
+    if (!p || !range_ok(p, lo, hi)) return ZERO3_EINVAL;
+    if (lo == hi) return ZERO3_OK;
+    if (!sparam || !full || !aligned16(full)) return ZERO3_EINVAL;
+    RankPtrs rp;
+    rp.full = full;
+    rp.in = reinterpret_cast<const void* const*>(sparam);
+    StreamArgs a;
+    zero3_status st = build_args(p, z3::kGather, rp, lo, hi, nullptr, 0, a);
+    if (st != ZERO3_OK) return st;
+    return cuda_status(z3::launch_stream(z3::kGather, a, stream));
+}
+
+zero3_status zero3_step(const zero3_plan* p, const zero3_adamw_hparams* hp, int64_t t,
+                        const uint16_t* const* grads, int64_t grads_origin, float* const* master,
+                        float* const* m, float* const* v, uint16_t* const* sparam,
+                        uint16_t* full, const zero3_persist_state* persist, int64_t lo,
+                        int64_t hi, zero3_stream stream) {
+    if (!p || !range_ok(p, lo, hi) || !hparams_ok(hp, t) || grads_origin > lo)
+        return ZERO3_EINVAL;
+    const z3::Scalars sc = step_scalars(p, hp, t);
+    if (lo < hi) {
+        if (!grads_ok(p, grads) || !sparam || !full || !aligned16(full)) return ZERO3_EINVAL;
+        RankPtrs rp;
+        rp.grads = grads;
+        rp.grads_origin = grads_origin;
+        rp.master = master;
+        rp.m = m;
+        rp.v = v;
+        rp.need_state = true;
+        rp.out = reinterpret_cast<void* const*>(sparam);
+        rp.full = full;
+        StreamArgs a;
+        zero3_status st = build_args(p, z3::kFused, rp, lo, hi, &sc, 0, a);
+        if (st != ZERO3_OK) return st;
+        // validate the persistent group before the first launch so that an
+        // error launches nothing
+        if (persist && !persist_ok(p, persist)) return ZERO3_EINVAL;
+        st = cuda_status(z3::launch_stream(z3::kFused, a, stream));
+        if (st != ZERO3_OK) return st;
+    }
+    if (persist) return persistent_launch(p, sc, persist, stream);
+    return ZERO3_OK;
+}
+
+zero3_status zero3_persistent_step(const zero3_plan* p, const zero3_adamw_hparams* hp, int64_t t,
+                                   const zero3_persist_state* persist, zero3_stream stream) {
+    if (!p || !hparams_ok(hp, t) || !persist) return ZERO3_EINVAL;
+    return persistent_launch(p, step_scalars(p, hp, t), persist, stream);
+}
+
+zero3_status zero3_cast_params(const zero3_plan* p, const float* const* master,
+                               uint16_t* const* sparam, uint16_t* full,
+                               const zero3_persist_state* persist, int64_t lo, int64_t hi,
+                               zero3_stream stream) {
+    if (!p || !range_ok(p, lo, hi)) return ZERO3_EINVAL;
+    if (full && !aligned16(full)) return ZERO3_EINVAL;
+    if (lo < hi) {
+        if (!master || !sparam) return ZERO3_EINVAL;
+        RankPtrs rp;
+        rp.full = full;
+        rp.out = reinterpret_cast<void* const*>(sparam);
+        rp.in = reinterpret_cast<const void* const*>(master);
+        StreamArgs a;
+        zero3_status st = build_args(p, z3::kCast, rp, lo, hi, nullptr, 0, a);
+        if (st != ZERO3_OK) return st;
+        st = cuda_status(z3::launch_stream(z3::kCast, a, stream));
+        if (st != ZERO3_OK) return st;
+    }
+    if (persist && p->psi_s > 0) {
+        if (!persist->master || !persist->param || !aligned16(persist->master) ||
+            !aligned16(persist->param))
+            return ZERO3_EINVAL;
+        StreamArgs a;
+        std::memset(&a, 0, sizeof(a));
+        a.nd = p->n_ranks;
+        Span s;
+        std::memset(&s, 0, sizeof(s));
+        s.lo = 0;
+        s.hi = p->psi_s;
+        s.fofs = -1;
+        s.in = persist->master;
+        s.out = persist->param;
+        s.vec = 1;
+        add_span(a, s);
+        return cuda_status(z3::launch_stream(z3::kCast, a, stream));
+    }
+    return ZERO3_OK;
+}
+
+// ------------------------------------------------------------- submodules
+
+zero3_status zero3_fetch_submodule(zero3_plan* p, int32_t k, const uint16_t* const* sparam,
+                                   const uint16_t* persist_param, uint16_t* out,
+                                   zero3_stream stream) {
+    if (!p || k < 0 || k >= static_cast<int32_t>(p->sub_tensors.size())) return ZERO3_EINVAL;
+    if (p->status[k] != ZERO3_NOT_AVAILABLE) {
+        if (out != p->fetched_out[k]) return ZERO3_ESTATE;
+        p->refs[k] += 1;
+        return ZERO3_OK;
+    }
+    const int64_t total = p->sub_numel[k];
+    if (total > 0 && (!out || !aligned16(out))) return ZERO3_EINVAL;
+    // Validate every source first so that an error launches nothing.
+    for (int64_t t : p->sub_tensors[k]) {
+        if (p->numel[t] == 0) continue;
+        if (p->persistent[t]) {
+            if (!persist_param || !aligned16(persist_param)) return ZERO3_EINVAL;
+        } else {
+            if (!sparam) return ZERO3_EINVAL;
+            for (int64_t s = p->seg_begin[t]; s < p->seg_begin[t + 1]; ++s) {
+                const uint16_t* src = sparam[p->segs[s].rank];
+                if (!src || !aligned16(src)) return ZERO3_EINVAL;
+            }
+        }
+    }
+    if (!p->events[k]) {
+        if (cudaEventCreateWithFlags(&p->events[k], cudaEventDisableTiming) != cudaSuccess) {
+            p->events[k] = nullptr;
+            return ZERO3_ECUDA;
+        }
+    }
+    z3::GatherArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.out = out;
+    int64_t running = 0;
+    auto flush = [&]() -> zero3_status {
+        zero3_status st = cuda_status(z3::launch_gather(a, stream));
+        a.n_segs = 0;
+        a.total_chunks = 0;
+        return st;
+    };
+    auto push = [&](const uint16_t* src, int64_t dst_off, int64_t len) -> zero3_status {
+        if (len <= 0) return ZERO3_OK;
+        if (a.n_segs == z3::kMaxGatherSegs) {
+            zero3_status st = flush();
+            if (st != ZERO3_OK) return st;
+        }
+        z3::GatherSeg& g = a.seg[a.n_segs++];
+        g.src = src;
+        g.dst_off = dst_off;
+        g.len = len;
+        g.chunk0 = a.total_chunks;
+        const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
+        g.vec = ((sa - 2u * static_cast<uintptr_t>(dst_off)) % 16u == 0) ? 1 : 0;
+        a.total_chunks += ((dst_off + len) - (dst_off & ~static_cast<int64_t>(7)) + 7) / 8;
+        return ZERO3_OK;
+    };
+    for (int64_t t : p->sub_tensors[k]) {
+        zero3_status st = ZERO3_OK;
+        if (p->persistent[t]) {
+            st = push(persist_param + p->offset[t], running, p->numel[t]);
+        } else {
+            for (int64_t s = p->seg_begin[t]; s < p->seg_begin[t + 1] && st == ZERO3_OK; ++s) {
+                const zero3_segment& sg = p->segs[s];
+                st = push(sparam[sg.rank] + sg.shard_off, running + sg.tensor_off, sg.len);
+            }
+        }
+        if (st != ZERO3_OK) return st;
+        running += p->numel[t];
+    }
+    if (a.n_segs > 0) {
+        zero3_status st = flush();
+        if (st != ZERO3_OK) return st;
+    }
+    if (cudaEventRecord(p->events[k], stream) != cudaSuccess) return ZERO3_ECUDA;
+    p->status[k] = ZERO3_INFLIGHT;
+    p->refs[k] = 1;
+    p->fetched_out[k] = out;
+    return ZERO3_OK;
+}
+
+zero3_status zero3_release_submodule(zero3_plan* p, int32_t k) {
+    if (!p || k < 0 || k >= static_cast<int32_t>(p->sub_tensors.size())) return ZERO3_EINVAL;
+    if (p->status[k] == ZERO3_NOT_AVAILABLE) return ZERO3_ESTATE;
+    p->refs[k] -= 1;
+    if (p->refs[k] == 0) {
+        p->status[k] = ZERO3_NOT_AVAILABLE;
+        p->fetched_out[k] = nullptr;
+    }
+    return ZERO3_OK;
+}
+
+zero3_status zero3_submodule_status(zero3_plan* p, int32_t k, int32_t* status) {
+    if (!p || !status || k < 0 || k >= static_cast<int32_t>(p->sub_tensors.size()))
+        return ZERO3_EINVAL;
+    if (p->status[k] == ZERO3_INFLIGHT) {
+        const cudaError_t e = cudaEventQuery(p->events[k]);
+        if (e == cudaSuccess)
+            p->status[k] = ZERO3_AVAILABLE;
+        else if (e != cudaErrorNotReady)
+            return ZERO3_ECUDA;
+    }
+    *status = p->status[k];
+    return ZERO3_OK;
+}
+
+zero3_status zero3_submodule_wait(zero3_plan* p, int32_t k) {
+    if (!p || k < 0 || k >= static_cast<int32_t>(p->sub_tensors.size())) return ZERO3_EINVAL;
+    if (p->status[k] == ZERO3_NOT_AVAILABLE) return ZERO3_ESTATE;
+    if (p->status[k] == ZERO3_INFLIGHT) {
+        if (cudaEventSynchronize(p->events[k]) != cudaSuccess) return ZERO3_ECUDA;
+        p->status[k] = ZERO3_AVAILABLE;
+    }
+    return ZERO3_OK;
+}
+
+zero3_status zero3_sync(zero3_stream stream) {
+    return cuda_status(cudaStreamSynchronize(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+// Internal declarations shared by the planner, the C ABI and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/zero3.h"
+
+struct zero3_plan {
+    int32_t n_ranks = 1;
+    int64_t threshold = 0;
+    int64_t bucket = 1;
+    std::vector<int64_t> numel;
+    std::vector<int32_t> submodule;
+    std::vector<uint8_t> persistent;
+    std::vector<int64_t> offset;
+    int64_t n_partitioned = 0;
+    int64_t psi_p = 0, psi_pad = 0, S = 0, psi_s = 0;
+    // segments of every tensor, concatenated; seg_begin[t]..seg_begin[t+1]
+    std::vector<zero3_segment> segs;
+    std::vector<int64_t> seg_begin;
+    // submodules: member tensors in list order
+    std::vector<std::vector<int64_t>> sub_tensors;
+    std::vector<int64_t> sub_numel;
+    // parameter state machine per submodule
+    std::vector<int32_t> status;
+    std::vector<int32_t> refs;
+    std::vector<uint16_t*> fetched_out;
+    std::vector<cudaEvent_t> events;
+};
+
+namespace z3 {
+
+// binary32 scalars of one AdamW step
+struct Scalars {
+    float decay, b1, omb1, b2, omb2, inv_sqrt_bc2, eps, step_size, inv_nd;
+};
+
+Scalars make_scalars(const zero3_adamw_hparams& hp, int64_t t, int32_t n_ranks);
+
+// Kernel modes of the streaming kernel.
+enum Mode : int {
+    kFused = 0,    // grads -> reduce -> AdamW -> sparam (+ full)
+    kReduce = 1,   // grads -> reduce -> shard grad (bf16 or f32)
+    kAdam = 2,     // shard grad -> AdamW -> sparam
+    kGather = 3,   // sparam -> full
+    kCast = 4,     // master -> sparam (+ full)
+};
+
+constexpr int kMaxSpans = ZERO3_MAX_RANKS;
+
+// One owner's slice of the requested range: local indices [lo, hi).
+struct Span {
+    int64_t lo, hi;
+    int64_t gofs;        // grads element offset of local index 0 (grads[q] + gofs + i)
+    int64_t fofs;        // full element offset of local index 0, or -1 (no full write)
+    int64_t chunk0;      // first 8-element chunk of this span in the launch's chunk space
+    float* master;
+    float* m;
+    float* v;
+    void* out;           // sparam (bf16) or shard grad (kReduce)
+    const void* in;      // shard grad (kAdam) or sparam (kGather) or master (kCast)
+    int32_t vec;         // 1 when full chunks may use 16-byte vector accesses
+    int32_t pad_;
+};
+
+struct StreamArgs {
+    const uint16_t* grads[ZERO3_MAX_RANKS];
+    uint16_t* full;
+    Span span[kMaxSpans];
+    int64_t total_chunks;
+    int32_t n_spans;
+    int32_t nd;
+    int32_t dtype;       // zero3_dtype of the shard grad (kReduce out / kAdam in)
+    int32_t pad_;
+    Scalars sc;
+};
+
+// Gather of submodule segments into a contiguous output.
+constexpr int kMaxGatherSegs = 64;
+struct GatherSeg {
+    const uint16_t* src;   // element 0 of the piece
+    int64_t dst_off;       // offset of the piece in out
+    int64_t len;
+    int64_t chunk0;
+    int32_t vec;
+    int32_t pad_;
+};
+struct GatherArgs {
+    uint16_t* out;
+    GatherSeg seg[kMaxGatherSegs];
+    int64_t total_chunks;
+    int32_t n_segs;
+    int32_t pad_;
+};
+
+cudaError_t launch_stream(int mode, const StreamArgs& a, cudaStream_t stream);
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream);
+
+}  // namespace z3

@@ -1,0 +1,349 @@
+// Streaming kernels of the ZeRO-3 step (sm_103a).
+//
+// Every kernel here is bound by HBM bandwidth: per element the fused step
+// reads N_d bf16 gradients and the fp32 master/m/v and writes master/m/v,
+// the bf16 shard and the bf16 all-gather copy, with about 20 binary32
+// operations in between.  There is no contraction, so no tensor core work.
+//
+// Work layout.  A launch covers up to ZERO3_MAX_RANKS "spans"; a span is one
+// owner's slice [lo, hi) of local indices (a rank's shard, or the persistent
+// group).  The spans' elements are cut into chunks of 8 consecutive local
+// indices aligned to multiples of 8, numbered consecutively across spans.
+// Thread c of the grid-stride loop takes chunk c, so the 32 lanes of a warp
+// touch 32 adjacent chunks: 512 contiguous bytes of every bf16 stream and
+// 1 KiB of every fp32 stream per warp instruction pair.  Interior chunks of a
+// span whose streams are all 16-byte aligned use 16-byte loads and stores;
+// the edge chunks of a span, and spans whose gradient or all-gather offsets
+// are not multiples of 8 elements, take the element-by-element path.
+//
+// Arithmetic per element follows the fixed order of the AdamW reading with
+// IEEE round-to-nearest intrinsics (no contraction into FMA):
+//   g = (sum_q f32(grad_q)) * inv_nd            (q ascending, from +0)
+//   p = p*decay; m = b1*m + omb1*g; v = b2*v + omb2*(g*g)
+//   d = sqrt(v)*inv_sqrt_bc2 + eps; p = p - step_size*(m/d); sparam = bf16(p)
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace z3 {
+
+// Kernel parameters are passed by value; 32764 bytes is the limit.
+static_assert(sizeof(StreamArgs) <= 32764, "StreamArgs exceeds the kernel parameter limit");
+static_assert(sizeof(GatherArgs) <= 32764, "GatherArgs exceeds the kernel parameter limit");
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float bf16_f32(uint16_t h) {
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// Two binary32 values -> packed bf16 pair, round to nearest even (hardware
+// conversion); `lo` lands in bits 0..15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ uint16_t to_bf16(float x) {
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void adamw(float g, float& p, float& m, float& v, const Scalars& s) {
+    p = __fmul_rn(p, s.decay);
+    m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
+    v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
+    const float d = __fadd_rn(__fmul_rn(__fsqrt_rn(v), s.inv_sqrt_bc2), s.eps);
+    p = __fsub_rn(p, __fmul_rn(s.step_size, __fdiv_rn(m, d)));
+}
+
+// Streaming (evict-first) 16-byte accesses: every byte is touched once.
+__device__ __forceinline__ uint4 ldcs16(const void* p) {
+    return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ float4 ldcs_f4(const float* p) {
+    return __ldcs(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ void stcs16(void* p, uint4 x) { __stcs(reinterpret_cast<uint4*>(p), x); }
+__device__ __forceinline__ void stcs_f4(float* p, float4 x) {
+    __stcs(reinterpret_cast<float4*>(p), x);
+}
+
+__device__ __forceinline__ void unpack8(const uint4& r, float* f) {
+    f[0] = bf16_lo(r.x); f[1] = bf16_hi(r.x);
+    f[2] = bf16_lo(r.y); f[3] = bf16_hi(r.y);
+    f[4] = bf16_lo(r.z); f[5] = bf16_hi(r.z);
+    f[6] = bf16_lo(r.w); f[7] = bf16_hi(r.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* f) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+}
+
+// Reduced gradient of 8 aligned elements, ranks summed in ascending order.
+template <int ND>
+__device__ __forceinline__ void reduce8(const StreamArgs& a, int64_t off, float* g) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) g[e] = 0.0f;
+    if constexpr (ND > 0) {
+        uint4 raw[ND];
+#pragma unroll
+        for (int q = 0; q < ND; ++q) raw[q] = ldcs16(a.grads[q] + off);
+#pragma unroll
+        for (int q = 0; q < ND; ++q) {
+            float f[8];
+            unpack8(raw[q], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) g[e] = __fadd_rn(g[e], f[e]);
+        }
+    } else {
+        const int nd = a.nd;
+        for (int q0 = 0; q0 < nd; q0 += 8) {
+            uint4 raw[8];
+            const int n = (nd - q0) < 8 ? (nd - q0) : 8;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (k < n) raw[k] = ldcs16(a.grads[q0 + k] + off);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (k < n) {
+                    float f[8];
+                    unpack8(raw[k], f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) g[e] = __fadd_rn(g[e], f[e]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) g[e] = __fmul_rn(g[e], a.sc.inv_nd);
+}
+
+template <int ND>
+__device__ __forceinline__ float reduce1(const StreamArgs& a, int64_t off) {
+    float s = 0.0f;
+    const int nd = ND > 0 ? ND : a.nd;
+    for (int q = 0; q < nd; ++q) s = __fadd_rn(s, bf16_f32(a.grads[q][off]));
+    return __fmul_rn(s, a.sc.inv_nd);
+}
+
+template <int MODE, int ND, int GT>
+__device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp, int64_t i0) {
+    float g[8];
+    if constexpr (MODE == kFused || MODE == kReduce) reduce8<ND>(a, sp.gofs + i0, g);
+
+    if constexpr (MODE == kReduce) {
+        if constexpr (GT == ZERO3_BF16) {
+            stcs16(static_cast<uint16_t*>(sp.out) + i0, pack8(g));
+        } else {
+            float* o = static_cast<float*>(sp.out) + i0;
+            stcs_f4(o, make_float4(g[0], g[1], g[2], g[3]));
+            stcs_f4(o + 4, make_float4(g[4], g[5], g[6], g[7]));
+        }
+        return;
+    }
+    if constexpr (MODE == kGather) {
+        const uint4 x = ldcs16(static_cast<const uint16_t*>(sp.in) + i0);
+        stcs16(a.full + sp.fofs + i0, x);
+        return;
+    }
+    if constexpr (MODE == kAdam) {
+        if constexpr (GT == ZERO3_BF16) {
+            unpack8(ldcs16(static_cast<const uint16_t*>(sp.in) + i0), g);
+        } else {
+            const float* in = static_cast<const float*>(sp.in) + i0;
+            const float4 g0 = ldcs_f4(in), g1 = ldcs_f4(in + 4);
+            g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
+            g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+        }
+    }
+    float p[8];
+    if constexpr (MODE == kCast) {
+        const float* in = static_cast<const float*>(sp.in) + i0;
+        const float4 p0 = ldcs_f4(in), p1 = ldcs_f4(in + 4);
+        p[0] = p0.x; p[1] = p0.y; p[2] = p0.z; p[3] = p0.w;
+        p[4] = p1.x; p[5] = p1.y; p[6] = p1.z; p[7] = p1.w;
+    } else {
+        float m[8], v[8];
+        const float4 p0 = ldcs_f4(sp.master + i0), p1 = ldcs_f4(sp.master + i0 + 4);
+        const float4 m0 = ldcs_f4(sp.m + i0), m1 = ldcs_f4(sp.m + i0 + 4);
+        const float4 v0 = ldcs_f4(sp.v + i0), v1 = ldcs_f4(sp.v + i0 + 4);
+        p[0] = p0.x; p[1] = p0.y; p[2] = p0.z; p[3] = p0.w;
+        p[4] = p1.x; p[5] = p1.y; p[6] = p1.z; p[7] = p1.w;
+        m[0] = m0.x; m[1] = m0.y; m[2] = m0.z; m[3] = m0.w;
+        m[4] = m1.x; m[5] = m1.y; m[6] = m1.z; m[7] = m1.w;
+        v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+        v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) adamw(g[e], p[e], m[e], v[e], a.sc);
+        stcs_f4(sp.master + i0, make_float4(p[0], p[1], p[2], p[3]));
+        stcs_f4(sp.master + i0 + 4, make_float4(p[4], p[5], p[6], p[7]));
+        stcs_f4(sp.m + i0, make_float4(m[0], m[1], m[2], m[3]));
+        stcs_f4(sp.m + i0 + 4, make_float4(m[4], m[5], m[6], m[7]));
+        stcs_f4(sp.v + i0, make_float4(v[0], v[1], v[2], v[3]));
+        stcs_f4(sp.v + i0 + 4, make_float4(v[4], v[5], v[6], v[7]));
+    }
+    const uint4 h = pack8(p);
+    stcs16(static_cast<uint16_t*>(sp.out) + i0, h);
+    if (sp.fofs >= 0) stcs16(a.full + sp.fofs + i0, h);
+}
+
+template <int MODE, int ND, int GT>
+__device__ __forceinline__ void scalar_chunk(const StreamArgs& a, const Span& sp, int64_t i0) {
+    for (int e = 0; e < 8; ++e) {
+        const int64_t i = i0 + e;
+        if (i < sp.lo || i >= sp.hi) continue;
+        float g = 0.0f;
+        if constexpr (MODE == kFused || MODE == kReduce) g = reduce1<ND>(a, sp.gofs + i);
+        if constexpr (MODE == kReduce) {
+            if constexpr (GT == ZERO3_BF16)
+                static_cast<uint16_t*>(sp.out)[i] = to_bf16(g);
+            else
+                static_cast<float*>(sp.out)[i] = g;
+            continue;
+        }
+        if constexpr (MODE == kGather) {
+            a.full[sp.fofs + i] = static_cast<const uint16_t*>(sp.in)[i];
+            continue;
+        }
+        if constexpr (MODE == kAdam) {
+            if constexpr (GT == ZERO3_BF16)
+                g = bf16_f32(static_cast<const uint16_t*>(sp.in)[i]);
+            else
+                g = static_cast<const float*>(sp.in)[i];
+        }
+        float p;
+        if constexpr (MODE == kCast) {
+            p = static_cast<const float*>(sp.in)[i];
+        } else {
+            p = sp.master[i];
+            float m = sp.m[i], v = sp.v[i];
+            adamw(g, p, m, v, a.sc);
+            sp.master[i] = p;
+            sp.m[i] = m;
+            sp.v[i] = v;
+        }
+        const uint16_t h = to_bf16(p);
+        static_cast<uint16_t*>(sp.out)[i] = h;
+        if (sp.fofs >= 0) a.full[sp.fofs + i] = h;
+    }
+}
+
+template <int MODE, int ND, int GT>
+__global__ void __launch_bounds__(kThreads) stream_kernel(const __grid_constant__ StreamArgs a) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int s = 0;
+    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+         c < a.total_chunks; c += stride) {
+        while (s + 1 < a.n_spans && c >= a.span[s + 1].chunk0) ++s;
+        const Span& sp = a.span[s];
+        const int64_t i0 = (sp.lo & ~static_cast<int64_t>(7)) + ((c - sp.chunk0) << 3);
+        if (sp.vec && i0 >= sp.lo && i0 + 8 <= sp.hi)
+            vector_chunk<MODE, ND, GT>(a, sp, i0);
+        else
+            scalar_chunk<MODE, ND, GT>(a, sp, i0);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherArgs a) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int s = 0;
+    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+         c < a.total_chunks; c += stride) {
+        while (s + 1 < a.n_segs && c >= a.seg[s + 1].chunk0) ++s;
+        const GatherSeg& g = a.seg[s];
+        const int64_t d0 = (g.dst_off & ~static_cast<int64_t>(7)) + ((c - g.chunk0) << 3);
+        const int64_t end = g.dst_off + g.len;
+        if (g.vec && d0 >= g.dst_off && d0 + 8 <= end) {
+            const uint4 x = ldcs16(g.src + (d0 - g.dst_off));
+            *reinterpret_cast<uint4*>(a.out + d0) = x;
+        } else {
+            for (int e = 0; e < 8; ++e) {
+                const int64_t d = d0 + e;
+                if (d >= g.dst_off && d < end) a.out[d] = g.src[d - g.dst_off];
+            }
+        }
+    }
+}
+
+// Grid-stride launches sized to fill every SM once at full occupancy.  The
+// per-device block count is cached per kernel (Tag makes each instantiation
+// own its cache).
+template <typename Tag, typename K>
+int grid_for(K kernel, int64_t total_chunks) {
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> cached[kMaxDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) dev = 0;
+    int blocks = cached[dev].load(std::memory_order_relaxed);
+    if (blocks <= 0) {
+        int sms = 0, per_sm = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+        if (per_sm < 1) per_sm = 1;
+        if (sms < 1) sms = 1;
+        blocks = sms * per_sm;
+        cached[dev].store(blocks, std::memory_order_relaxed);
+    }
+    const int64_t need = (total_chunks + kThreads - 1) / kThreads;
+    return static_cast<int>(need < blocks ? need : blocks);
+}
+
+template <int MODE, int ND, int GT>
+struct StreamTag {};
+struct GatherTag {};
+
+template <int MODE, int ND, int GT>
+cudaError_t launch_one(const StreamArgs& a, cudaStream_t stream) {
+    auto k = stream_kernel<MODE, ND, GT>;
+    const int grid = grid_for<StreamTag<MODE, ND, GT>>(k, a.total_chunks);
+    if (grid > 0) k<<<grid, kThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int MODE, int GT>
+cudaError_t launch_nd(const StreamArgs& a, cudaStream_t stream) {
+    switch (a.nd) {
+        case 1: return launch_one<MODE, 1, GT>(a, stream);
+        case 2: return launch_one<MODE, 2, GT>(a, stream);
+        case 4: return launch_one<MODE, 4, GT>(a, stream);
+        case 8: return launch_one<MODE, 8, GT>(a, stream);
+        default: return launch_one<MODE, 0, GT>(a, stream);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_stream(int mode, const StreamArgs& a, cudaStream_t stream) {
+    if (a.total_chunks <= 0) return cudaSuccess;
+    switch (mode) {
+        case kFused: return launch_nd<kFused, 0>(a, stream);
+        case kReduce:
+            return a.dtype == ZERO3_BF16 ? launch_nd<kReduce, ZERO3_BF16>(a, stream)
+                                         : launch_nd<kReduce, ZERO3_F32>(a, stream);
+        case kAdam:
+            return a.dtype == ZERO3_BF16 ? launch_one<kAdam, 1, ZERO3_BF16>(a, stream)
+                                         : launch_one<kAdam, 1, ZERO3_F32>(a, stream);
+        case kGather: return launch_one<kGather, 1, 0>(a, stream);
+        case kCast: return launch_one<kCast, 1, 0>(a, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream) {
+    if (a.total_chunks <= 0) return cudaSuccess;
+    const int grid = grid_for<GatherTag>(gather_kernel, a.total_chunks);
+    gather_kernel<<<grid, kThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace z3

@@ -1,0 +1,179 @@
+"""N_d virtual data-parallel ranks laid out in one GPU's HBM.
+
+Allocation and call plumbing only: PyTorch allocates the buffers, the seeded
+device generator fills the inputs, and every step of the path is a call into
+libzero3 through the `zero3` binding.
+
+Layout (all separate allocations, each 512-byte aligned by the allocator):
+  grads[c][q]   bf16  rank q's local gradient for flat range chunk c
+                      (chunk c = [lo_c, hi_c); index f at grads[c][q][f - lo_c])
+  pgrads[q]     bf16  rank q's local gradient of the persistent group (psi_s)
+  master/m/v[r] fp32  rank r's optimizer-state shard (S), only for state ranks
+  sparam[r]     bf16  rank r's parameter shard (S), every rank
+  full          bf16  the flat all-gathered parameter buffer (psi_pad)
+  pmaster/pm/pv fp32, pparam bf16: the one resident copy of the persistent group
+  out           bf16  the submodule gather buffer (largest submodule)
+"""
+from __future__ import annotations
+
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import synth_device, zero3
+from .workloads import (STREAM_GRAD, STREAM_GRAD_PERSIST, STREAM_MASTER,
+                        STREAM_MASTER_PERSIST, Workload)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> int:
+    return t.data_ptr() if t is not None else 0
+
+
+class Emulation:
+    def __init__(self, w: Workload, device: str = "cuda", state_ranks: Optional[Sequence[int]] = None,
+                 bucketed: bool = False, stream: Optional[torch.cuda.Stream] = None,
+                 alloc_grads: bool = True):
+        self.w = w
+        self.dev = torch.device(device)
+        self.plan = zero3.Plan(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+        info = self.plan.info
+        self.nd = w.n_ranks
+        self.S = info.shard_len
+        self.psi_p, self.psi_pad, self.psi_s = info.psi_p, info.psi_pad, info.psi_s
+        self.state_ranks = list(range(self.nd)) if state_ranks is None else sorted(state_ranks)
+        self.hp = zero3.hparams(**w.hparams)
+        self.stream = stream
+        # flat range whose owners hold optimizer state on this device
+        lo = min(self.state_ranks) * self.S
+        hi = (max(self.state_ranks) + 1) * self.S
+        assert self.state_ranks == list(range(min(self.state_ranks), max(self.state_ranks) + 1)), \
+            "state ranks must be consecutive"
+        if bucketed:
+            cuts = sorted({lo, hi} | {b for b in range(0, self.psi_pad, w.bucket) if lo < b < hi})
+            self.chunks = list(zip(cuts[:-1], cuts[1:]))
+        else:
+            self.chunks = [(lo, hi)] if hi > lo else []
+        e = dict(device=self.dev)
+        bf, f32 = torch.bfloat16, torch.float32
+        self.grads: List[List[torch.Tensor]] = []
+        if alloc_grads:
+            for (a, b) in self.chunks:
+                self.grads.append([torch.empty(b - a, dtype=bf, **e) for _ in range(self.nd)])
+        self.pgrads = [torch.empty(self.psi_s, dtype=bf, **e) for _ in range(self.nd)]
+        self.master: List[Optional[torch.Tensor]] = [None] * self.nd
+        self.m: List[Optional[torch.Tensor]] = [None] * self.nd
+        self.v: List[Optional[torch.Tensor]] = [None] * self.nd
+        for r in self.state_ranks:
+            self.master[r] = torch.empty(self.S, dtype=f32, **e)
+            self.m[r] = torch.zeros(self.S, dtype=f32, **e)
+            self.v[r] = torch.zeros(self.S, dtype=f32, **e)
+        self.sparam = [torch.empty(self.S, dtype=bf, **e) for _ in range(self.nd)]
+        self.full = torch.zeros(self.psi_pad, dtype=bf, **e)
+        self.pmaster = torch.empty(self.psi_s, dtype=f32, **e)
+        self.pm = torch.zeros(self.psi_s, dtype=f32, **e)
+        self.pv = torch.zeros(self.psi_s, dtype=f32, **e)
+        self.pparam = torch.empty(self.psi_s, dtype=bf, **e)
+        self.max_sub = max([self.plan.submodule(k)[1] for k in range(info.n_submodules)] + [0])
+        self.out = torch.empty(max(self.max_sub, 1), dtype=bf, **e)
+        self.persist = zero3.persist_state([_ptr(g) for g in self.pgrads], _ptr(self.pmaster),
+                                           _ptr(self.pm), _ptr(self.pv), _ptr(self.pparam))
+
+    # ------------------------------------------------------------ plumbing
+    @property
+    def sid(self) -> int:
+        s = self.stream if self.stream is not None else torch.cuda.current_stream(self.dev)
+        return s.cuda_stream
+
+    def ptrs(self, xs) -> List[int]:
+        return [_ptr(x) for x in xs]
+
+    # ------------------------------------------------------------ inputs
+    def init_params(self) -> None:
+        """fp32 masters from the generator (padding zero), m = v = 0, then the
+        bf16 shards, the full buffer and the persistent params via
+        zero3_cast_params.  Shards of ranks without state are cast from a
+        temporary master."""
+        w = self.w
+        for r in range(self.nd):
+            tmp = self.master[r] if self.master[r] is not None else \
+                torch.empty(self.S, dtype=torch.float32, device=self.dev)
+            n = max(0, min(self.S, self.psi_p - r * self.S))
+            if self.S > n:
+                tmp[n:].zero_()
+            synth_device.normal(_ptr(tmp), n, seed=w.seed, stream_id=STREAM_MASTER, step=0, rank=0,
+                                index0=r * self.S, sigma=w.master_sigma, bf16=False,
+                                cuda_stream=self.sid)
+            masters = [0] * self.nd
+            sparams = [0] * self.nd
+            masters[r] = _ptr(tmp)
+            sparams[r] = _ptr(self.sparam[r])
+            zero3.zero3_cast_params(self.plan, masters, sparams, _ptr(self.full), None,
+                                    r * self.S, (r + 1) * self.S, self.sid)
+        synth_device.normal(_ptr(self.pmaster), self.psi_s, seed=w.seed,
+                            stream_id=STREAM_MASTER_PERSIST, step=0, rank=0, index0=0,
+                            sigma=w.master_sigma, bf16=False, cuda_stream=self.sid)
+        zero3.zero3_cast_params(self.plan, None, None, 0, self.persist, 0, 0, self.sid)
+
+    def fill_grads(self, step: int) -> None:
+        """Every rank's local gradient for `step` from the generator; the
+        padding [psi_p, psi_pad) is zero."""
+        w = self.w
+        for (a, b), G in zip(self.chunks, self.grads):
+            n = max(0, min(b, self.psi_p) - a)
+            for q in range(self.nd):
+                if b - a > n:
+                    G[q][n:].zero_()
+                synth_device.normal(_ptr(G[q]), n, seed=w.seed, stream_id=STREAM_GRAD, step=step,
+                                    rank=q, index0=a, sigma=w.grad_sigma, outlier_p=w.outlier_p,
+                                    outlier_sigma=w.outlier_sigma, cuda_stream=self.sid)
+        for q in range(self.nd):
+            synth_device.normal(_ptr(self.pgrads[q]), self.psi_s, seed=w.seed,
+                                stream_id=STREAM_GRAD_PERSIST, step=step, rank=q, index0=0,
+                                sigma=w.grad_sigma, outlier_p=w.outlier_p,
+                                outlier_sigma=w.outlier_sigma, cuda_stream=self.sid)
+
+    # ------------------------------------------------------------ the path
+    def step(self, t: int, with_persistent: bool = True) -> None:
+        """The fused ZeRO-3 step over every chunk (one launch per chunk) and
+        the persistent group."""
+        for c, ((a, b), G) in enumerate(zip(self.chunks, self.grads)):
+            zero3.zero3_step(self.plan, self.hp, t, self.ptrs(G), a, self.ptrs(self.master),
+                             self.ptrs(self.m), self.ptrs(self.v), self.ptrs(self.sparam),
+                             _ptr(self.full), self.persist if (with_persistent and c == 0) else None,
+                             a, b, self.sid)
+        if with_persistent and not self.chunks:
+            zero3.zero3_persistent_step(self.plan, self.hp, t, self.persist, self.sid)
+
+    def fetch(self, k: int) -> None:
+        zero3.zero3_fetch_submodule(self.plan, k, self.ptrs(self.sparam), _ptr(self.pparam),
+                                    _ptr(self.out), self.sid)
+
+    def release(self, k: int) -> None:
+        zero3.zero3_release_submodule(self.plan, k)
+
+    def forward_backward_gathers(self) -> None:
+        """Gather every submodule before its forward (list order) and again
+        before its backward (reverse order), releasing after each use."""
+        n = self.plan.info.n_submodules
+        for k in range(n):
+            self.fetch(k)
+            self.release(k)
+        for k in reversed(range(n)):
+            self.fetch(k)
+            self.release(k)
+
+    def full_step(self, t: int) -> None:
+        self.forward_backward_gathers()
+        self.step(t)
+
+    # ------------------------------------------------------------ accounting
+    def step_bytes(self) -> dict:
+        """Algorithmic HBM bytes of one full step (fused step + persistent +
+        two gathers of every submodule)."""
+        nd = self.nd
+        n_flat = sum(b - a for a, b in self.chunks)
+        fused = n_flat * (2 * nd + 24 + 2 + 2)
+        persist = self.psi_s * (2 * nd + 24 + 2)
+        gathers = 2 * sum(self.plan.submodule(k)[1] for k in range(self.plan.info.n_submodules)) * 4
+        return dict(fused=fused, persistent=persist, gathers=gathers,
+                    total=fused + persist + gathers, flat_elems=n_flat)

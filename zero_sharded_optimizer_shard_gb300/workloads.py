@@ -190,9 +190,11 @@ def ragged(n_tensors: int = 2000, n_ranks: int = 7, seed: int = 3,
 
 
 def ragged_small(n_ranks: int = 7) -> Workload:
-    """Ragged list scaled down so the whole oracle runs in seconds (same recipe,
-    200 tensors, big sizes in [1e5, 4e5])."""
-    w = ragged(n_tensors=200, n_ranks=n_ranks, big_hi=4e5)
+    """The ragged recipe scaled down so the whole oracle runs in seconds:
+    300 tensors, persistence threshold 1e3, sizes a 30/70 mixture of
+    log-uniform [1, 1e3) and [1e3, 4e4]."""
+    w = ragged(n_tensors=300, n_ranks=n_ranks, small_hi=1e3, big_lo=1e3, big_hi=4e4)
+    w.threshold = 1000
     w.name = f"ragged_small_nd{n_ranks}"
     return w
 

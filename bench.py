@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decoder_1p3b")
+    ap.add_argument("--n-ranks", type=int, default=None,
+                    help="override the workload's N_d (small profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -82,10 +84,12 @@ def kernels_sha() -> str:
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 50 ms; stop() keeps the samples taken inside
+    the timed window [t0, t1] (host clock)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -96,47 +100,58 @@ class ClockSampler:
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
+            self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0: float, t1: float):
+        import datetime
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        self.out.close()
         rows = []
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) >= 9:
-                rows.append(parts)
-        os.unlink(self.path)
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = set()
-        sm, smax, pw = [], [], []
-        for r in rows:
+            if len(parts) < 10:
+                continue
             try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
-                pw.append(float(r[3]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]),
+                             [parts[6 + k].lower().startswith("active") for k in range(4)]))
             except ValueError:
                 continue
-            for k, name in enumerate(names):
-                if r[5 + k].lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(pw) if pw else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        window = "timed region"
+        if not inside:  # timed region shorter than the sampling interval
+            inside = [r for r in rows if t0 - 0.1 <= r[0] <= t1 + 0.1]
+            window = "timed region +-100 ms"
+        reasons = sorted({n for r in inside for n, a in zip(self.NAMES, r[4]) if a})
+        return {"sm_mhz": statistics.median(r[1] for r in inside) if inside else None,
+                "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+                "power_w_max": max(r[3] for r in inside) if inside else None,
+                "samples": len(inside), "window": window, "reasons": reasons}
 
 
-def cpu_oracle_rate(wname: str, budget_s: float = 15.0):
+def make_workload(args):
+    from zero_sharded_optimizer_shard_gb300 import workloads as W
+    fac = WORKLOADS[args.workload][0]
+    w = W.llama_7b() if fac == "llama_7b_rank0" else getattr(W, fac)()
+    if args.n_ranks:
+        w.n_ranks = args.n_ranks
+    return w
+
+
+def cpu_oracle_rate(w, budget_s: float = 15.0):
     """The CPU oracle, as it stands, on a bounded contiguous sample of rank
     0's shard: all N_d ranks' gradients for the sample, the reduce, AdamW and
     bf16 cast.  Returns (params/s, description)."""
@@ -145,7 +160,6 @@ def cpu_oracle_rate(wname: str, budget_s: float = 15.0):
     import oracle as O
     from zero_sharded_optimizer_shard_gb300 import synth, workloads as W
 
-    w = getattr(W, WORKLOADS[wname][0])() if wname != "llama_7b_rank0" else W.llama_7b()
     plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
     rng_n = 1 << 20
     idx = np.arange(rng_n, dtype=np.int64)
@@ -183,7 +197,7 @@ def run_reference(args):
     rates = []
     desc = None
     for i in range(args.warmup + args.steps):
-        r, desc, _ = cpu_oracle_rate(args.workload, budget_s=budget)
+        r, desc, _ = cpu_oracle_rate(make_workload(args), budget_s=budget)
         if i >= args.warmup:
             rates.append(r)
     value = sum(rates) / len(rates)
@@ -200,6 +214,21 @@ def run_reference(args):
     }
     print(json.dumps(line))
     return 0
+
+
+def reduce_max(value: float, device) -> float:
+    """Max of a per-rank value over the process group (barrier included)."""
+    import torch
+    import torch.distributed as dist
+    x = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(x, op=dist.ReduceOp.MAX)
+    return float(x.item())
+
+
+def replica_throughput(world: int, params_per_replica: int, ms_per_step: float) -> float:
+    """Weak scaling: every replica processes its own copy of the workload, so
+    the job's params/s is world x params / the slowest rank's step time."""
+    return world * params_per_replica / (ms_per_step / 1e3)
 
 
 def launches_per_step(e) -> int:
@@ -238,7 +267,9 @@ def run_ours(args):
     from zero_sharded_optimizer_shard_gb300.emulation import Emulation
 
     fac, state_ranks, bucketed, desc = WORKLOADS[args.workload]
-    w = getattr(W, fac)() if fac != "llama_7b_rank0" else W.llama_7b()
+    w = make_workload(args)
+    if args.n_ranks:
+        desc += f" (N_d overridden to {w.n_ranks})"
     stream = torch.cuda.Stream()
     e = Emulation(w, device=f"cuda:{local}", state_ranks=state_ranks, bucketed=bucketed,
                   stream=stream)
@@ -268,13 +299,14 @@ def run_ours(args):
 
     clocks = ClockSampler(local)
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.5)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    tw0 = time.time()
     wall0 = time.perf_counter()
     start.record(stream)
     for k in range(args.steps):
@@ -283,25 +315,22 @@ def run_ours(args):
     end.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    tw1 = time.time()
     if world > 1:
         dist.barrier()
     ms = start.elapsed_time(end)
     fused_ms = [a.elapsed_time(b) for a, b in evs]
-    clk = clocks.stop()
+    clk = clocks.stop(tw0, tw1)
     if world > 1:
-        x = torch.tensor([ms], device=f"cuda:{local}", dtype=torch.float64)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        ms = float(x.item())
+        ms = reduce_max(ms, f"cuda:{local}")
 
     # ---- end to end through the public API: host gradients in, params out
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(e, w, args, stream, n_params, t)
-        if world > 1 and e2e is not None:
-            x = torch.tensor([e2e["ms_per_step"]], device=f"cuda:{local}", dtype=torch.float64)
-            dist.all_reduce(x, op=dist.ReduceOp.MAX)
-            e2e["value"] = world * n_params / (float(x.item()) / 1e3)
-            e2e["ms_per_step"] = float(x.item())
+        if world > 1 and e2e is not None and e2e.get("ms_per_step"):
+            e2e["ms_per_step"] = reduce_max(e2e["ms_per_step"], f"cuda:{local}")
+            e2e["value"] = replica_throughput(world, n_params, e2e["ms_per_step"])
 
     if rank == 0:
         ms_step = ms / args.steps
@@ -311,13 +340,13 @@ def run_ours(args):
         achieved = fused_bytes_launch / (fused_launch_ms / 1e3) / 1e9
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            rate, sample, _ = cpu_oracle_rate(args.workload, budget_s=15.0)
+            rate, sample, _ = cpu_oracle_rate(w, budget_s=15.0)
             cpu = {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
                    "sample": sample}
         step_gbs = nbytes["total"] / (ms_step / 1e3) / 1e9
         line = {
             "metric": METRIC,
-            "value": world * n_params / (ms_step / 1e3),
+            "value": replica_throughput(world, n_params, ms_step),
             "unit": "params/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_step,

@@ -10,13 +10,16 @@ from zero_sharded_optimizer_shard_gb300.workloads import (STREAM_GRAD, STREAM_GR
                                                           STREAM_MASTER, STREAM_MASTER_PERSIST)
 
 
+def host_master_persist(w, plan):
+    return synth.normal_f32(w.seed, STREAM_MASTER_PERSIST, 0, 0, np.arange(plan.psi_s),
+                            w.master_sigma)
+
+
 def host_master(w, plan):
     mf = np.zeros(plan.psi_pad, np.float32)
     mf[:plan.psi_p] = synth.normal_f32(w.seed, STREAM_MASTER, 0, 0, np.arange(plan.psi_p),
                                        w.master_sigma)
-    mp = synth.normal_f32(w.seed, STREAM_MASTER_PERSIST, 0, 0, np.arange(plan.psi_s),
-                          w.master_sigma)
-    return mf, mp
+    return mf, host_master_persist(w, plan)
 
 
 def host_grads(w, plan, t, idx=None):
@@ -67,6 +70,22 @@ def sampled_oracle(w, plan, idx, T, grad_step=None):
         gs = t if grad_step is None else grad_step
         sc = O.adamw_scalars(w.hparams, t, plan.n_ranks)
         g = O.reduce_sum(host_grads(w, plan, gs, idx), sc["inv_nd"])
+        p, m, v = O.adamw_update(g, p, m, v, sc)
+    return p, m, v, O.cast_bf16(p)
+
+
+def sampled_persistent_oracle(w, plan, pidx, T, grad_step=None):
+    """Persistent-group oracle at persistent indices pidx only."""
+    pidx = np.asarray(pidx, np.int64)
+    p = synth.normal_f32(w.seed, STREAM_MASTER_PERSIST, 0, 0, pidx, w.master_sigma)
+    m = np.zeros_like(p)
+    v = np.zeros_like(p)
+    for t in range(1, T + 1):
+        gs = t if grad_step is None else grad_step
+        sc = O.adamw_scalars(w.hparams, t, plan.n_ranks)
+        g = O.reduce_sum([synth.normal_bf16(w.seed, STREAM_GRAD_PERSIST, gs, q, pidx, w.grad_sigma,
+                                            w.outlier_p, w.outlier_sigma)
+                          for q in range(plan.n_ranks)], sc["inv_nd"])
         p, m, v = O.adamw_update(g, p, m, v, sc)
     return p, m, v, O.cast_bf16(p)
 

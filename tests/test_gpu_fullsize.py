@@ -1,0 +1,200 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+benchmark uses, on sampled outputs the oracle computes one by one
+(elementwise independence of the update), plus the whole persistent group.
+
+Sample: random flat indices plus every rank's first and last two local
+indices, tensor boundaries and the padding."""
+import gc
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle as O  # noqa: E402
+from tests._oracle_runs import (assert_bf16_close, assert_f32_close, bits, f32,  # noqa: E402
+                                host_master_persist, host_pgrads, sampled_oracle,
+                                sampled_persistent_oracle, u16)
+from zero_sharded_optimizer_shard_gb300 import workloads as W  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _free_memory():
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def sample_indices(plan, lo, hi, n, seed):
+    rng = np.random.default_rng(seed)
+    S = plan.shard_len
+    idx = set(int(x) for x in rng.integers(lo, hi, n))
+    for r in range(plan.n_ranks):
+        for f in (r * S, r * S + 1, (r + 1) * S - 2, (r + 1) * S - 1):
+            if lo <= f < hi:
+                idx.add(f)
+    for t in range(len(plan.numel)):
+        if not plan.persistent[t]:
+            for f in (plan.offset[t], plan.offset[t] + plan.numel[t] - 1):
+                if lo <= f < hi:
+                    idx.add(f)
+    for f in range(plan.psi_p, plan.psi_pad):
+        if lo <= f < hi:
+            idx.add(f)
+    return np.array(sorted(idx), np.int64)
+
+
+def persistent_oracle(w, plan, T, grad_step=None):
+    mp = host_master_persist(w, plan)
+    ps = O.PersistState(mp.copy(), np.zeros_like(mp), np.zeros_like(mp), O.cast_bf16(mp))
+    for t in range(1, T + 1):
+        O.persistent_step(plan, w.hparams, t, host_pgrads(w, plan, t if grad_step is None else grad_step),
+                          ps, replicas=2)
+    return ps
+
+
+def check_sample(e, plan, w, idx, T, grad_step=None):
+    p, m, v, h = sampled_oracle(w, plan, idx, T, grad_step)
+    S = plan.shard_len
+    r = idx // S
+    i = idx % S
+    gm = np.empty(len(idx), np.float32)
+    gmm = np.empty(len(idx), np.float32)
+    gv = np.empty(len(idx), np.float32)
+    gs = np.empty(len(idx), np.uint16)
+    for q in np.unique(r):
+        sel = r == q
+        ii = torch.from_numpy(i[sel]).to(e.master[q].device)
+        gm[sel] = f32(e.master[q][ii])
+        gmm[sel] = f32(e.m[q][ii])
+        gv[sel] = f32(e.v[q][ii])
+        gs[sel] = u16(e.sparam[q][ii])
+    gfull = u16(e.full[torch.from_numpy(idx).to(e.full.device)])
+    for name, got, ref in (("master", gm, p), ("m", gmm, m), ("v", gv, v)):
+        assert_f32_close(got, ref, what=name)
+        assert np.array_equal(bits(got), bits(ref)), f"{name} not bit-exact"
+    assert_bf16_close(gs, h, what="sparam")
+    assert np.array_equal(gs, h) and np.array_equal(gfull, h)
+
+
+def check_persistent(e, ps):
+    for name, got, ref in (("pmaster", e.pmaster, ps.master), ("pm", e.pm, ps.m), ("pv", e.pv, ps.v)):
+        g = f32(got)
+        assert_f32_close(g, ref, what=name)
+        assert np.array_equal(bits(g), bits(ref)), name
+    assert np.array_equal(u16(e.pparam), ps.param)
+
+
+def run(w, T, grad_step=None, **kw):
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+    e = Emulation(w, **kw)
+    e.init_params()
+    for t in range(1, T + 1):
+        if grad_step is None or t == 1:
+            e.fill_grads(t if grad_step is None else grad_step)
+        e.full_step(t)
+    torch.cuda.synchronize()
+    return e
+
+
+def check_fetch(e, plan, w, T, grad_step, ks, ps, n=4000, seed=0):
+    """Gathered submodule outputs at sampled positions against the oracle's
+    bf16 parameters of the same flat / persistent elements."""
+    rng = np.random.default_rng(seed)
+    for k in ks:
+        e.fetch(k)
+        torch.cuda.synchronize()
+        members = plan.submodules[k]
+        pos, flat, pers = [], [], []
+        base = 0
+        for t in members:
+            nt = plan.numel[t]
+            js = np.unique(np.concatenate([rng.integers(0, nt, min(nt, n // len(members) + 1)),
+                                           [0, nt - 1]]))
+            for j in js:
+                pos.append(base + j)
+                if plan.persistent[t]:
+                    flat.append(-1)
+                    pers.append(plan.offset[t] + j)
+                else:
+                    flat.append(plan.offset[t] + j)
+                    pers.append(-1)
+            base += nt
+        pos, flat, pers = np.array(pos), np.array(flat), np.array(pers)
+        got = u16(e.out[torch.from_numpy(pos).to(e.out.device)])
+        want = np.empty(len(pos), np.uint16)
+        fsel = flat >= 0
+        if fsel.any():
+            want[fsel] = sampled_oracle(w, plan, flat[fsel], T, grad_step)[3]
+        if (~fsel).any():
+            want[~fsel] = ps.param[pers[~fsel]]
+        assert np.array_equal(got, want), f"submodule {k}"
+        e.release(k)
+
+
+def test_gpt2_small_ten_steps():
+    w = W.gpt2_small()
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    e = run(w, 10)
+    check_sample(e, plan, w, sample_indices(plan, 0, plan.psi_pad, 150_000, 1), 10)
+    ps = persistent_oracle(w, plan, 10)
+    check_persistent(e, ps)
+    check_fetch(e, plan, w, 10, None, [0, 5, plan.n_submodules - 1], ps)
+
+
+def test_decoder_1p3b_bench_configuration():
+    """The benchmark's workload and launch configuration: full emulation of
+    N_d = 8 ranks, one fused launch over the whole flat range, gradients
+    generated once and reused by every step."""
+    w = W.decoder_1p3b()
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    T = 3
+    e = run(w, T, grad_step=1)
+    check_sample(e, plan, w, sample_indices(plan, 0, plan.psi_pad, 120_000, 2), T, grad_step=1)
+    ps = persistent_oracle(w, plan, T, grad_step=1)
+    check_persistent(e, ps)
+    check_fetch(e, plan, w, T, 1, [0, 12, plan.n_submodules - 1], ps)
+
+
+def test_llama_7b_rank0_view():
+    """Rank 0's state only, gradients in 5e8-element bucket buffers (two
+    launches per step), bf16 all-gather into the 6.7B-element full buffer."""
+    w = W.llama_7b()
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    T = 2
+    e = run(w, T, state_ranks=[0], bucketed=True)
+    assert len(e.chunks) == 2
+    check_sample(e, plan, w, sample_indices(plan, 0, plan.shard_len, 100_000, 3), T)
+    ps = persistent_oracle(w, plan, T)
+    check_persistent(e, ps)
+
+
+def test_ragged_2000_full():
+    """2000 ragged tensors, N_d = 7: shard offsets not multiples of 8 (element
+    path), padding, shards crossing tensors, per-submodule fetch."""
+    w = W.ragged()
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    T = 5
+    e = run(w, T)
+    check_sample(e, plan, w, sample_indices(plan, 0, plan.psi_pad, 100_000, 4), T)
+    # persistent group (~5M elements) on a sample, ends included
+    rng = np.random.default_rng(5)
+    pidx = np.unique(np.concatenate([rng.integers(0, plan.psi_s, 50_000), [0, plan.psi_s - 1]]))
+    p, m, v, h = sampled_persistent_oracle(w, plan, pidx, T)
+    sel = torch.from_numpy(pidx).to(e.pmaster.device)
+    for name, got, ref in (("pmaster", e.pmaster, p), ("pm", e.pm, m), ("pv", e.pv, v)):
+        g = f32(got[sel])
+        assert_f32_close(g, ref, what=name)
+        assert np.array_equal(bits(g), bits(ref)), name
+    assert np.array_equal(u16(e.pparam[sel]), h)
+    # fetch: persistent members of the checked submodules come from the same sample set
+    ps_param = np.zeros(plan.psi_s, np.uint16)
+    ks = [0, 100, plan.n_submodules - 1]
+    need = [np.arange(plan.offset[t], plan.offset[t] + plan.numel[t])
+            for k in ks for t in plan.submodules[k] if plan.persistent[t]]
+    if need:
+        need = np.unique(np.concatenate(need))
+        ps_param[need] = sampled_persistent_oracle(w, plan, need, T)[3]
+    check_fetch(e, plan, w, T, None, ks, O.PersistState(None, None, None, ps_param))

@@ -121,7 +121,7 @@ def test_rank0_view_matches_oracle(dev):
 
 def test_padding_stays_exactly_zero(dev):
     w = W.ragged_small(7)
-    plan = O.partition(w.numels, w.submodule_of, 7)
+    plan = O.partition(w.numels, w.submodule_of, 7, w.threshold, w.bucket)
     assert plan.psi_pad > plan.psi_p
     e = run_device(w, 3)
     S = e.S

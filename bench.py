@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decoder_1p3b")
     ap.add_argument("--n-ranks", type=int, default=None,
                     help="override the workload's N_d (small profiling cases)")
+    ap.add_argument("--stage", type=int, choices=[2, 3], default=3,
+                    help="3: ZeRO-3 step (default); 2: the ZeRO-1/2 step (full parameters on "
+                         "every rank, no submodule gathers)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -148,6 +151,8 @@ def make_workload(args):
     w = W.llama_7b() if fac == "llama_7b_rank0" else getattr(W, fac)()
     if args.n_ranks:
         w.n_ranks = args.n_ranks
+    if args.stage == 2:
+        w.threshold = 0  # the persistence threshold is a stage-3 setting
     return w
 
 
@@ -246,6 +251,71 @@ def launches_per_step(e) -> int:
             pieces += 1 if ti.persistent else ti.n_segments
         n += 2 * math.ceil(pieces / 64)
     return n + len(e.chunks) + (1 if e.psi_s > 0 else 0)
+
+
+def run_stage12(args):
+    """The ZeRO-1/2 step: every rank keeps full bf16 parameters, so a step is
+    the fused reduce-scatter + AdamW + all-gather into all N_d copies."""
+    import torch
+    from zero_sharded_optimizer_shard_gb300 import build as b
+    b.build_all(quiet=True)
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+    torch.cuda.set_device(0)
+    fac, state_ranks, bucketed, desc = WORKLOADS[args.workload]
+    if state_ranks is not None:
+        raise SystemExit("--stage 2 needs a full emulation workload")
+    w = make_workload(args)
+    stream = torch.cuda.Stream()
+    e = Emulation(w, stream=stream)
+    with torch.cuda.stream(stream):
+        e.init_params()
+        e.fill_grads(1)
+        params = [e.full.clone() for _ in range(w.n_ranks)]
+    e.sparam = e.full = None  # stage 1/2 keeps no separate shard or gathered buffer
+    torch.cuda.synchronize()
+    pp = [x.data_ptr() for x in params]
+    lo, hi = e.chunks[0]
+
+    def step(t):
+        zero3.zero3_step_stage12(e.plan, e.hp, t, e.ptrs(e.grads[0]), lo, e.ptrs(e.master),
+                                 e.ptrs(e.m), e.ptrs(e.v), pp, lo, hi, e.sid)
+
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        step(t)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.5)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    tw0 = time.time()
+    start.record(stream)
+    for _ in range(args.steps):
+        t += 1
+        step(t)
+    end.record(stream)
+    torch.cuda.synchronize()
+    tw1 = time.time()
+    ms = start.elapsed_time(end) / args.steps
+    clk = clocks.stop(tw0, tw1)
+    n_el = hi - lo
+    bpe = 4 * w.n_ranks + 24
+    peak, peak_kind = peaks()
+    achieved = n_el * bpe / (ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": METRIC, "value": w.psi / (ms / 1e3), "unit": "params/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": desc + ", ZeRO-1/2 step (full bf16 parameters on every rank)",
+                   "name": args.workload, "stage": "1/2", "n_ranks": w.n_ranks, "params": w.psi,
+                   "bytes_per_elem": bpe},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "kernel": "stream_kernel<kFusedRep, N_d> (zero3_step_stage12)"},
+        "gpu_launches": args.steps, "clocks": clk, "cpu_baseline": None, "e2e": None}))
+    return 0
 
 
 def run_ours(args):
@@ -435,6 +505,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.stage == 2:
+        return run_stage12(args)
     return run_ours(args)
 
 

@@ -47,7 +47,8 @@ typedef enum zero3_status {
     ZERO3_EINVAL = 1, /* bad argument: NULL/misaligned pointer, bad range, size, id */
     ZERO3_ESTATE = 2, /* call not allowed in the submodule's current state */
     ZERO3_ECUDA = 3,  /* CUDA runtime error, including an earlier asynchronous fault */
-    ZERO3_ENOMEM = 4  /* host allocation failed */
+    ZERO3_ENOMEM = 4, /* host allocation failed */
+    ZERO3_EIO = 5     /* checkpoint file missing, short, or written for another partition */
 } zero3_status;
 
 typedef enum zero3_dtype { ZERO3_BF16 = 0, ZERO3_F32 = 1 } zero3_dtype;
@@ -220,6 +221,24 @@ zero3_status zero3_step(const zero3_plan* plan, const zero3_adamw_hparams* hp, i
                         const zero3_persist_state* persist,
                         int64_t flat_lo, int64_t flat_hi, zero3_stream stream);
 
+/* The ZeRO-1 / ZeRO-2 step: parameters are not partitioned and every rank
+ * keeps the full 2-byte parameters ([compass] Stage 1 and Stage 2
+ * mechanisms; [111qqz] sections "ZeRO-1" and "ZeRO-2").  Same reduce-scatter
+ * and AdamW on each rank's fp32 shard as zero3_step, then the updated bf16
+ * values are written into EVERY rank's full copy: params[q][f] for all
+ * q = 0..N_d-1 and every flat f in the range (the all-gather that restores
+ * consistency after the sharded update).  params: host array of N_d device
+ * pointers, each psi_pad bf16 elements.  Stages 1 and 2 share this step;
+ * they differ in the gradient memory a rank keeps (see zero3_memory_bytes).
+ * Per element it moves 2*N_d + 24 + 2*N_d bytes.  Create the plan with
+ * persistence threshold 0 (the threshold is a stage-3 setting); persistent
+ * tensors, if any, are updated by zero3_persistent_step. */
+zero3_status zero3_step_stage12(const zero3_plan* plan, const zero3_adamw_hparams* hp, int64_t t,
+                                const uint16_t* const* grads, int64_t grads_origin,
+                                float* const* master, float* const* m, float* const* v,
+                                uint16_t* const* params, int64_t flat_lo, int64_t flat_hi,
+                                zero3_stream stream);
+
 /* Update of the unpartitioned group alone ([hotelren], 小参数驻留: small
  * parameters stay resident and are not partitioned): the same fixed-order
  * sum times 1/N_d of the ranks' gradients and the same AdamW as above on the
@@ -266,6 +285,49 @@ zero3_status zero3_submodule_status(zero3_plan* plan, int32_t k, int32_t* status
 
 /* Blocks the host until submodule k's gather has finished; marks AVAILABLE. */
 zero3_status zero3_submodule_wait(zero3_plan* plan, int32_t k);
+
+/* ------------------------------------------------------------ checkpoints
+ * Each partition is saved and restored by itself ([cnhsyj] section 4.3:
+ * save_checkpoint / load_checkpoint write and read every partition), or the
+ * weights are gathered into complete 16-bit tensors on save ([hotelren],
+ * stage3_gather_16bit_weights_on_model_save; [baike] section 应用).
+ * A file is a 48-byte header (magic "ZERO3CKP", version 1, kind, rank,
+ * n_ranks, element count, step t, fingerprint of the partition: rank count,
+ * threshold and every tensor's element count) followed by raw little-endian
+ * arrays.  Loading checks every header field against the plan and the
+ * arguments and returns ZERO3_EIO on any mismatch, on a short file or on
+ * trailing bytes; nothing is written to device memory before the header has
+ * been validated.  Calls are synchronous (they synchronise `stream`); device
+ * pointers need no alignment except `full` (16 bytes).  The library stages
+ * through a 16 MiB host buffer that it allocates and frees per call. */
+
+/* Writes rank `rank`'s fp32 master, m and v shards (S elements each) and the
+ * step count t. */
+zero3_status zero3_save_shard(const zero3_plan* plan, int32_t rank, int64_t t, const float* master,
+                              const float* m, const float* v, const char* path,
+                              zero3_stream stream);
+
+/* Restores a shard written by zero3_save_shard for the same rank and
+ * partition; *t receives the saved step count.  After loading every rank,
+ * zero3_cast_params rebuilds the bf16 shards and the full buffer. */
+zero3_status zero3_load_shard(const zero3_plan* plan, int32_t rank, int64_t* t, float* master,
+                              float* m, float* v, const char* path, zero3_stream stream);
+
+/* Same for the persistent group's fp32 master, m and v (psi_s each);
+ * persist->grads and persist->param are not used. */
+zero3_status zero3_save_persistent(const zero3_plan* plan, int64_t t,
+                                   const zero3_persist_state* persist, const char* path,
+                                   zero3_stream stream);
+zero3_status zero3_load_persistent(const zero3_plan* plan, int64_t* t,
+                                   const zero3_persist_state* persist, const char* path,
+                                   zero3_stream stream);
+
+/* Consolidated 16-bit weights: every tensor in list order, complete, as bf16
+ * (partitioned tensors read from the all-gathered `full` buffer, persistent
+ * ones from persist_param).  Element count in the header = psi_p + psi_s. */
+zero3_status zero3_save_16bit_weights(const zero3_plan* plan, const uint16_t* full,
+                                      const uint16_t* persist_param, const char* path,
+                                      zero3_stream stream);
 
 /* ------------------------------------------------------------- accounting */
 

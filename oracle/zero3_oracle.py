@@ -17,7 +17,9 @@ What it computes, with the passages each part follows:
 * ddp_step      -- the unsharded data-parallel step (all-reduce, then the full
                    AdamW on every replica) that the sharded step must equal.
 * persistent_step -- the unpartitioned (persistent) group, updated DDP style.
+* replicated_step -- the ZeRO-1/2 step: every rank keeps full parameters.
 * fetch_submodule -- gather a submodule's shards into one contiguous tensor.
+* gather_16bit_weights -- every tensor complete, in list order (save).
 * memory_bytes, comm_elems, ring_send_bytes -- the model-state and
                    communication accounting.
 
@@ -361,6 +363,25 @@ def sharded_step(plan: Plan, hp: dict, t: int, grads: Sequence[np.ndarray],
     full[lo:hi] = gathered[lo:hi]
 
 
+def replicated_step(plan: Plan, hp: dict, t: int, grads: Sequence[np.ndarray],
+                    st: ShardState, params: Sequence[np.ndarray],
+                    flat_lo: int = 0, flat_hi: Optional[int] = None) -> None:
+    """ZeRO-1 / ZeRO-2 step, in place: parameters are not partitioned, every
+    rank keeps the full 2-byte parameters (ZeRO concept page, Stage 1/2
+    mechanism; "ddp-to-zero-memory-sharding", sections "ZeRO-1" and
+    "ZeRO-2").  Reduce-scatter the gradients, update each rank's fp32 slice,
+    write it back to 2 bytes, then all-gather the updated slices into every
+    rank's full copy params[q].  Stages 1 and 2 compute the same step; they
+    differ in which gradient memory a rank keeps (the full local gradient vs
+    its reduced slice), see memory_bytes."""
+    if flat_hi is None:
+        flat_hi = plan.psi_pad
+    full = allgather(plan, st.sparam).copy()
+    sharded_step(plan, hp, t, grads, st, full, flat_lo, flat_hi)
+    for q in range(plan.n_ranks):
+        params[q][flat_lo:flat_hi] = full[flat_lo:flat_hi]
+
+
 def persistent_step(plan: Plan, hp: dict, t: int, pgrads: Sequence[np.ndarray],
                     ps: PersistState, replicas: Optional[int] = None) -> None:
     """Update of the unpartitioned (persistent) group, in place.
@@ -450,6 +471,32 @@ def fetch_submodule(plan: Plan, k: int, sparam: Sequence[np.ndarray],
                     out[sel] = np.asarray(sparam[r])[f[sel] - r * S]
             parts.append(out)
     return np.concatenate(parts) if parts else np.zeros(0, np.uint16)
+
+
+def gather_16bit_weights(plan: Plan, sparam: Sequence[np.ndarray],
+                         persist_param: np.ndarray) -> List[np.ndarray]:
+    """Consolidated 16-bit weights: every tensor complete, in list order,
+    gathered from the owning shards or the persistent copy.  Saving a ZeRO-3
+    model as full weights needs this gather because each rank holds only
+    disjoint fragments (encyclopedia entry, section 应用;
+    "DeepSpeed Zero-3 的参数分区与按需访问机制",
+    stage3_gather_16bit_weights_on_model_save)."""
+    S = plan.shard_len
+    out = []
+    for t in range(len(plan.numel)):
+        n = plan.numel[t]
+        if plan.persistent[t]:
+            o = plan.offset[t]
+            out.append(np.asarray(persist_param[o:o + n], np.uint16).copy())
+        else:
+            f = np.arange(plan.offset[t], plan.offset[t] + n, dtype=np.int64)
+            w = np.empty(n, np.uint16)
+            for r in range(plan.n_ranks):
+                sel = (f // S) == r
+                if sel.any():
+                    w[sel] = np.asarray(sparam[r])[f[sel] - r * S]
+            out.append(w)
+    return out
 
 
 class SubmoduleStates:

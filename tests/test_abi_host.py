@@ -20,7 +20,7 @@ HEADER = os.path.join(ROOT, "include", "zero3.h")
 def header_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(zero3_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(zero3_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_lists_every_binding_function():
@@ -225,3 +225,44 @@ def test_status_strings(lib):
     assert zero3.status_string(zero3.OK) == "ok"
     assert "invalid" in zero3.status_string(zero3.EINVAL)
     assert zero3.status_string(99) == "unknown status"
+
+
+# ---------------------------------------------------------------- checkpoint headers
+def _header(kind=1, rank=0, n_ranks=2, n_elems=None, t=5, fp=None, magic=b"ZERO3CKP", version=1,
+            plan=None):
+    import struct
+    return struct.pack("<8sIIiiqqQ", magic, version, kind, rank, n_ranks,
+                       n_elems if n_elems is not None else plan.info.shard_len, t,
+                       fp if fp is not None else 0)
+
+
+def test_checkpoint_load_rejects_bad_files(lib, tmp_path):
+    """Every header mismatch is reported as ZERO3_EIO before any device memory
+    is touched (the device pointers here are fake)."""
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    p = _plan()
+    t = C.c_int64()
+    cases = {
+        "missing": None,
+        "short": b"ZERO3C",
+        "magic": _header(magic=b"NOTZERO3", plan=p),
+        "fingerprint": _header(fp=12345, plan=p),
+        "version": _header(version=2, plan=p),
+        "kind": _header(kind=3, plan=p),
+        "rank": _header(rank=1, plan=p),
+        "n_elems": _header(n_elems=7, plan=p),
+    }
+    for name, data in cases.items():
+        path = tmp_path / f"{name}.ckpt"
+        if data is not None:
+            path.write_bytes(data)
+        st = zero3.raw_status("zero3_load_shard", p.handle, 0, C.byref(t), FAKE, FAKE, FAKE,
+                              str(path).encode(), None)
+        assert st == zero3.EIO, name
+    # argument errors come first
+    assert zero3.raw_status("zero3_load_shard", p.handle, 2, C.byref(t), FAKE, FAKE, FAKE,
+                            b"x", None) == zero3.EINVAL
+    assert zero3.raw_status("zero3_save_shard", p.handle, 0, -1, FAKE, FAKE, FAKE, b"x",
+                            None) == zero3.EINVAL
+    assert zero3.raw_status("zero3_save_16bit_weights", p.handle, MISALIGNED, FAKE, b"x",
+                            None) == zero3.EINVAL

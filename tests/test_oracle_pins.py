@@ -256,6 +256,25 @@ def test_sharded_equals_ddp_bitwise(nd):
         assert np.array_equal(full, ddp.param[0])
 
 
+@pytest.mark.parametrize("nd", [2, 3, 8])
+def test_stage12_replicas_equal_ddp(nd):
+    """ZeRO-1/2: after every step each rank's full parameter copy equals the
+    DDP replicas' parameters (the all-gather restores consistency:
+    "ddp-to-zero-memory-sharding", section "ZeRO-1")."""
+    numels = [1000, 37, 5, 2300, 999, 64]
+    plan, mf, _ = _random_problem(numels, nd, seed=12, threshold=0)
+    st, full, _ = O.init_state(plan, mf, np.zeros(0, np.float32))
+    params = [full.copy() for _ in range(nd)]
+    ddp = O.ddp_init(plan, mf)
+    for t in range(1, 4):
+        G = _grads(plan, 12, t, nd)
+        O.replicated_step(plan, HP, t, G, st, params)
+        O.ddp_step(plan, HP, t, G, ddp)
+        for q in range(nd):
+            assert np.array_equal(params[q], ddp.param[q])
+        assert np.array_equal(np.concatenate(st.master).view(np.uint32), ddp.master[0].view(np.uint32))
+
+
 def test_padding_stays_zero():
     plan, mf, _ = _random_problem([1001, 13], 4, seed=5, threshold=0)
     assert plan.psi_pad - plan.psi_p == 2
@@ -357,6 +376,9 @@ def test_partition_brute_force(nd):
         for t in range(n_t):
             got = O.fetch_submodule(plan, t, sparam, pp)
             assert np.array_equal(got, vals[t])
+        # consolidated 16-bit weights: every tensor complete, in list order
+        whole = O.gather_16bit_weights(plan, sparam, pp)
+        assert len(whole) == n_t and all(np.array_equal(a, b) for a, b in zip(whole, vals))
 
 
 def test_workload_sizes():

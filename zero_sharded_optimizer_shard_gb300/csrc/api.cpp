@@ -244,6 +244,33 @@ zero3_status zero3_step(const zero3_plan* p, const zero3_adamw_hparams* hp, int6
     return ZERO3_OK;
 }
 
+zero3_status zero3_step_stage12(const zero3_plan* p, const zero3_adamw_hparams* hp, int64_t t,
+                                const uint16_t* const* grads, int64_t grads_origin,
+                                float* const* master, float* const* m, float* const* v,
+                                uint16_t* const* params, int64_t lo, int64_t hi,
+                                zero3_stream stream) {
+    if (!p || !range_ok(p, lo, hi) || !hparams_ok(hp, t) || grads_origin > lo)
+        return ZERO3_EINVAL;
+    if (lo == hi) return ZERO3_OK;
+    if (!grads_ok(p, grads) || !params) return ZERO3_EINVAL;
+    for (int q = 0; q < p->n_ranks; ++q)
+        if (!params[q] || !aligned16(params[q])) return ZERO3_EINVAL;
+    const z3::Scalars sc = step_scalars(p, hp, t);
+    RankPtrs rp;
+    rp.grads = grads;
+    rp.grads_origin = grads_origin;
+    rp.master = master;
+    rp.m = m;
+    rp.v = v;
+    rp.need_state = true;
+    rp.full = params[0];  // every copy has the same layout: offsets and phase
+    StreamArgs a;
+    zero3_status st = build_args(p, z3::kFusedRep, rp, lo, hi, &sc, 0, a);
+    if (st != ZERO3_OK) return st;
+    for (int q = 0; q < p->n_ranks; ++q) a.reps[q] = params[q];
+    return cuda_status(z3::launch_stream(z3::kFusedRep, a, stream));
+}
+
 zero3_status zero3_persistent_step(const zero3_plan* p, const zero3_adamw_hparams* hp, int64_t t,
                                    const zero3_persist_state* persist, zero3_stream stream) {
     if (!p || !hparams_ok(hp, t) || !persist) return ZERO3_EINVAL;

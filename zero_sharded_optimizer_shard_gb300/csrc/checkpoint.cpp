@@ -1,0 +1,231 @@
+// Checkpoints of the sharded state and the consolidated 16-bit weights.
+//
+// Under ZeRO-3 each rank's state is a disjoint fragment, so checkpoints are
+// saved per partition and restored by the same partitioning (ZERO tutorial,
+// cnhsyj.com, section 4.3: save_checkpoint writes every partition,
+// load_checkpoint restores them), or the weights are gathered into complete
+// 16-bit tensors at save time ("DeepSpeed Zero-3 的参数分区与按需访问机制",
+// stage3_gather_16bit_weights_on_model_save; encyclopedia entry
+// "DeepSpeed ZeRO-3", section 应用: either gather full weights or save the
+// shards and merge them later).
+//
+// File = header + raw little-endian arrays.  The header carries a fingerprint
+// of the partition (rank count, threshold, element counts), so a shard can
+// only be loaded into the partitioning that wrote it.
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "internal.h"
+
+namespace {
+
+constexpr char kMagic[8] = {'Z', 'E', 'R', 'O', '3', 'C', 'K', 'P'};
+constexpr uint32_t kVersion = 1;
+enum Kind : uint32_t { kShard = 1, kPersist = 2, kWeights16 = 3 };
+constexpr int64_t kStage = int64_t(16) << 20;  // bytes per host staging chunk
+
+struct Header {
+    char magic[8];
+    uint32_t version;
+    uint32_t kind;
+    int32_t rank;
+    int32_t n_ranks;
+    int64_t n_elems;
+    int64_t t;
+    uint64_t fingerprint;
+};
+static_assert(sizeof(Header) == 48, "checkpoint header layout");
+
+// FNV-1a over the values that fix the partition.
+uint64_t fingerprint(const zero3_plan* p) {
+    uint64_t h = 1469598103934665603ull;
+    auto mix = [&h](int64_t x) {
+        for (int k = 0; k < 8; ++k) {
+            h ^= static_cast<uint64_t>((x >> (8 * k)) & 0xff);
+            h *= 1099511628211ull;
+        }
+    };
+    mix(p->n_ranks);
+    mix(p->threshold);
+    mix(static_cast<int64_t>(p->numel.size()));
+    for (int64_t n : p->numel) mix(n);
+    return h;
+}
+
+Header make_header(const zero3_plan* p, Kind kind, int32_t rank, int64_t n, int64_t t) {
+    Header h;
+    std::memcpy(h.magic, kMagic, 8);
+    h.version = kVersion;
+    h.kind = kind;
+    h.rank = rank;
+    h.n_ranks = p->n_ranks;
+    h.n_elems = n;
+    h.t = t;
+    h.fingerprint = fingerprint(p);
+    return h;
+}
+
+struct File {
+    FILE* f = nullptr;
+    ~File() {
+        if (f) std::fclose(f);
+    }
+};
+
+// Copies `bytes` of device memory at src to the file through a host buffer.
+zero3_status write_device(FILE* f, const void* src, int64_t bytes, std::vector<char>& buf,
+                          cudaStream_t s) {
+    const char* p = static_cast<const char*>(src);
+    for (int64_t off = 0; off < bytes; off += kStage) {
+        const int64_t n = (bytes - off) < kStage ? (bytes - off) : kStage;
+        if (cudaMemcpyAsync(buf.data(), p + off, n, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return ZERO3_ECUDA;
+        if (std::fwrite(buf.data(), 1, n, f) != static_cast<size_t>(n)) return ZERO3_EIO;
+    }
+    return ZERO3_OK;
+}
+
+zero3_status read_device(FILE* f, void* dst, int64_t bytes, std::vector<char>& buf,
+                         cudaStream_t s) {
+    char* p = static_cast<char*>(dst);
+    for (int64_t off = 0; off < bytes; off += kStage) {
+        const int64_t n = (bytes - off) < kStage ? (bytes - off) : kStage;
+        if (std::fread(buf.data(), 1, n, f) != static_cast<size_t>(n)) return ZERO3_EIO;
+        if (cudaMemcpyAsync(p + off, buf.data(), n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return ZERO3_ECUDA;
+    }
+    return ZERO3_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Opens and validates a checkpoint file written for this plan.
+zero3_status open_checked(const zero3_plan* p, const char* path, Kind kind, int32_t rank,
+                          int64_t n, File& file, Header& h) {
+    file.f = std::fopen(path, "rb");
+    if (!file.f) return ZERO3_EIO;
+    if (std::fread(&h, sizeof(h), 1, file.f) != 1) return ZERO3_EIO;
+    if (std::memcmp(h.magic, kMagic, 8) != 0 || h.version != kVersion || h.kind != kind ||
+        h.rank != rank || h.n_ranks != p->n_ranks || h.n_elems != n ||
+        h.fingerprint != fingerprint(p) || h.t < 0)
+        return ZERO3_EIO;
+    return ZERO3_OK;
+}
+
+zero3_status save_arrays(const zero3_plan* p, const char* path, Kind kind, int32_t rank,
+                         int64_t n, int64_t t, const void* const* arrays, int n_arrays,
+                         int elem_bytes, cudaStream_t s) {
+    File file;
+    file.f = std::fopen(path, "wb");
+    if (!file.f) return ZERO3_EIO;
+    const Header h = make_header(p, kind, rank, n, t);
+    if (std::fwrite(&h, sizeof(h), 1, file.f) != 1) return ZERO3_EIO;
+    std::vector<char> buf;
+    try {
+        buf.resize(kStage);
+    } catch (const std::bad_alloc&) {
+        return ZERO3_ENOMEM;
+    }
+    for (int k = 0; k < n_arrays; ++k) {
+        zero3_status st = write_device(file.f, arrays[k], n * elem_bytes, buf, s);
+        if (st != ZERO3_OK) return st;
+    }
+    if (std::fflush(file.f) != 0) return ZERO3_EIO;
+    return ZERO3_OK;
+}
+
+zero3_status load_arrays(const zero3_plan* p, const char* path, Kind kind, int32_t rank,
+                         int64_t n, int64_t* t, void* const* arrays, int n_arrays,
+                         int elem_bytes, cudaStream_t s) {
+    File file;
+    Header h;
+    zero3_status st = open_checked(p, path, kind, rank, n, file, h);
+    if (st != ZERO3_OK) return st;
+    std::vector<char> buf;
+    try {
+        buf.resize(kStage);
+    } catch (const std::bad_alloc&) {
+        return ZERO3_ENOMEM;
+    }
+    for (int k = 0; k < n_arrays; ++k) {
+        st = read_device(file.f, arrays[k], n * elem_bytes, buf, s);
+        if (st != ZERO3_OK) return st;
+    }
+    char extra;
+    if (std::fread(&extra, 1, 1, file.f) != 0) return ZERO3_EIO;  // trailing bytes
+    *t = h.t;
+    return ZERO3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+zero3_status zero3_save_shard(const zero3_plan* p, int32_t rank, int64_t t, const float* master,
+                              const float* m, const float* v, const char* path,
+                              zero3_stream stream) {
+    if (!p || !path || rank < 0 || rank >= p->n_ranks || t < 0) return ZERO3_EINVAL;
+    if (p->S > 0 && (!master || !m || !v)) return ZERO3_EINVAL;
+    const void* arrays[3] = {master, m, v};
+    return save_arrays(p, path, kShard, rank, p->S, t, arrays, 3, 4, stream);
+}
+
+zero3_status zero3_load_shard(const zero3_plan* p, int32_t rank, int64_t* t, float* master,
+                              float* m, float* v, const char* path, zero3_stream stream) {
+    if (!p || !path || !t || rank < 0 || rank >= p->n_ranks) return ZERO3_EINVAL;
+    if (p->S > 0 && (!master || !m || !v)) return ZERO3_EINVAL;
+    void* arrays[3] = {master, m, v};
+    return load_arrays(p, path, kShard, rank, p->S, t, arrays, 3, 4, stream);
+}
+
+zero3_status zero3_save_persistent(const zero3_plan* p, int64_t t,
+                                   const zero3_persist_state* ps, const char* path,
+                                   zero3_stream stream) {
+    if (!p || !path || !ps || t < 0) return ZERO3_EINVAL;
+    if (p->psi_s > 0 && (!ps->master || !ps->m || !ps->v)) return ZERO3_EINVAL;
+    const void* arrays[3] = {ps->master, ps->m, ps->v};
+    return save_arrays(p, path, kPersist, -1, p->psi_s, t, arrays, 3, 4, stream);
+}
+
+zero3_status zero3_load_persistent(const zero3_plan* p, int64_t* t,
+                                   const zero3_persist_state* ps, const char* path,
+                                   zero3_stream stream) {
+    if (!p || !path || !ps || !t) return ZERO3_EINVAL;
+    if (p->psi_s > 0 && (!ps->master || !ps->m || !ps->v)) return ZERO3_EINVAL;
+    void* arrays[3] = {ps->master, ps->m, ps->v};
+    return load_arrays(p, path, kPersist, -1, p->psi_s, t, arrays, 3, 4, stream);
+}
+
+zero3_status zero3_save_16bit_weights(const zero3_plan* p, const uint16_t* full,
+                                      const uint16_t* persist_param, const char* path,
+                                      zero3_stream stream) {
+    if (!p || !path) return ZERO3_EINVAL;
+    if (p->psi_p > 0 && (!full || !aligned16(full))) return ZERO3_EINVAL;
+    if (p->psi_s > 0 && !persist_param) return ZERO3_EINVAL;
+    File file;
+    file.f = std::fopen(path, "wb");
+    if (!file.f) return ZERO3_EIO;
+    const int64_t total = p->psi_p + p->psi_s;
+    const Header h = make_header(p, kWeights16, -1, total, 0);
+    if (std::fwrite(&h, sizeof(h), 1, file.f) != 1) return ZERO3_EIO;
+    std::vector<char> buf;
+    try {
+        buf.resize(kStage);
+    } catch (const std::bad_alloc&) {
+        return ZERO3_ENOMEM;
+    }
+    // Tensors in list order; a partitioned tensor is contiguous in the flat
+    // all-gathered buffer, a persistent one in the persistent copy.
+    for (size_t t = 0; t < p->numel.size(); ++t) {
+        const uint16_t* src = (p->persistent[t] ? persist_param : full) + p->offset[t];
+        zero3_status st = write_device(file.f, src, p->numel[t] * 2, buf, stream);
+        if (st != ZERO3_OK) return st;
+    }
+    if (std::fflush(file.f) != 0) return ZERO3_EIO;
+    return ZERO3_OK;
+}
+
+}  // extern "C"

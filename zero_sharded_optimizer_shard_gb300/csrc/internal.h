@@ -47,6 +47,7 @@ enum Mode : int {
     kAdam = 2,     // shard grad -> AdamW -> sparam
     kGather = 3,   // sparam -> full
     kCast = 4,     // master -> sparam (+ full)
+    kFusedRep = 5, // grads -> reduce -> AdamW -> every rank's full copy (ZeRO-1/2)
 };
 
 constexpr int kMaxSpans = ZERO3_MAX_RANKS;
@@ -68,6 +69,7 @@ struct Span {
 
 struct StreamArgs {
     const uint16_t* grads[ZERO3_MAX_RANKS];
+    uint16_t* reps[ZERO3_MAX_RANKS];   // kFusedRep: every rank's full parameter copy
     uint16_t* full;
     Span span[kMaxSpans];
     int64_t total_chunks;

@@ -138,7 +138,8 @@ __device__ __forceinline__ float reduce1(const StreamArgs& a, int64_t off) {
 template <int MODE, int ND, int GT>
 __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp, int64_t i0) {
     float g[8];
-    if constexpr (MODE == kFused || MODE == kReduce) reduce8<ND>(a, sp.gofs + i0, g);
+    if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kReduce)
+        reduce8<ND>(a, sp.gofs + i0, g);
 
     if constexpr (MODE == kReduce) {
         if constexpr (GT == ZERO3_BF16) {
@@ -192,8 +193,18 @@ __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp
         stcs_f4(sp.v + i0 + 4, make_float4(v[4], v[5], v[6], v[7]));
     }
     const uint4 h = pack8(p);
-    stcs16(static_cast<uint16_t*>(sp.out) + i0, h);
-    if (sp.fofs >= 0) stcs16(a.full + sp.fofs + i0, h);
+    if constexpr (MODE == kFusedRep) {
+        // all-gather into every rank's full parameter copy
+        const int nd = ND > 0 ? ND : a.nd;
+#pragma unroll
+        for (int q = 0; q < (ND > 0 ? ND : ZERO3_MAX_RANKS); ++q) {
+            if (ND == 0 && q >= nd) break;
+            stcs16(a.reps[q] + sp.fofs + i0, h);
+        }
+    } else {
+        stcs16(static_cast<uint16_t*>(sp.out) + i0, h);
+        if (sp.fofs >= 0) stcs16(a.full + sp.fofs + i0, h);
+    }
 }
 
 template <int MODE, int ND, int GT>
@@ -202,7 +213,8 @@ __device__ __forceinline__ void scalar_chunk(const StreamArgs& a, const Span& sp
         const int64_t i = i0 + e;
         if (i < sp.lo || i >= sp.hi) continue;
         float g = 0.0f;
-        if constexpr (MODE == kFused || MODE == kReduce) g = reduce1<ND>(a, sp.gofs + i);
+        if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kReduce)
+            g = reduce1<ND>(a, sp.gofs + i);
         if constexpr (MODE == kReduce) {
             if constexpr (GT == ZERO3_BF16)
                 static_cast<uint16_t*>(sp.out)[i] = to_bf16(g);
@@ -232,8 +244,13 @@ __device__ __forceinline__ void scalar_chunk(const StreamArgs& a, const Span& sp
             sp.v[i] = v;
         }
         const uint16_t h = to_bf16(p);
-        static_cast<uint16_t*>(sp.out)[i] = h;
-        if (sp.fofs >= 0) a.full[sp.fofs + i] = h;
+        if constexpr (MODE == kFusedRep) {
+            const int nd = ND > 0 ? ND : a.nd;
+            for (int q = 0; q < nd; ++q) a.reps[q][sp.fofs + i] = h;
+        } else {
+            static_cast<uint16_t*>(sp.out)[i] = h;
+            if (sp.fofs >= 0) a.full[sp.fofs + i] = h;
+        }
     }
 }
 
@@ -309,6 +326,7 @@ cudaError_t launch_stream(int mode, const StreamArgs& a, cudaStream_t stream) {
     if (a.total_chunks <= 0) return cudaSuccess;
     switch (mode) {
         case kFused: return launch_nd<kFused, 0>(a, stream);
+        case kFusedRep: return launch_nd<kFusedRep, 0>(a, stream);
         case kReduce:
             return a.dtype == ZERO3_BF16 ? launch_nd<kReduce, ZERO3_BF16>(a, stream)
                                          : launch_nd<kReduce, ZERO3_F32>(a, stream);

@@ -241,6 +241,7 @@ const char* zero3_status_string(zero3_status s) {
         case ZERO3_ESTATE: return "invalid submodule state";
         case ZERO3_ECUDA: return "CUDA error";
         case ZERO3_ENOMEM: return "out of host memory";
+        case ZERO3_EIO: return "checkpoint file error";
     }
     return "unknown status";
 }

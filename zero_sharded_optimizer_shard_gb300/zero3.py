@@ -16,7 +16,7 @@ from typing import Optional, Sequence
 
 from .build import lib_path
 
-OK, EINVAL, ESTATE, ECUDA, ENOMEM = 0, 1, 2, 3, 4
+OK, EINVAL, ESTATE, ECUDA, ENOMEM, EIO = 0, 1, 2, 3, 4, 5
 BF16, F32 = 0, 1
 NOT_AVAILABLE, INFLIGHT, AVAILABLE = 0, 1, 2
 MAX_RANKS = 64
@@ -83,6 +83,9 @@ _SIGS = [
     ("zero3_step", C.c_int, [_vp, C.POINTER(AdamWHparams), C.c_int64, C.POINTER(_vp), C.c_int64,
                              C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp), _vp,
                              C.POINTER(PersistState), C.c_int64, C.c_int64, _vp]),
+    ("zero3_step_stage12", C.c_int, [_vp, C.POINTER(AdamWHparams), C.c_int64, C.POINTER(_vp),
+                                     C.c_int64, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp),
+                                     C.POINTER(_vp), C.c_int64, C.c_int64, _vp]),
     ("zero3_persistent_step", C.c_int, [_vp, C.POINTER(AdamWHparams), C.c_int64,
                                         C.POINTER(PersistState), _vp]),
     ("zero3_cast_params", C.c_int, [_vp, C.POINTER(_vp), C.POINTER(_vp), _vp,
@@ -91,6 +94,11 @@ _SIGS = [
     ("zero3_release_submodule", C.c_int, [_vp, C.c_int32]),
     ("zero3_submodule_status", C.c_int, [_vp, C.c_int32, _c_i32_p]),
     ("zero3_submodule_wait", C.c_int, [_vp, C.c_int32]),
+    ("zero3_save_shard", C.c_int, [_vp, C.c_int32, C.c_int64, _vp, _vp, _vp, C.c_char_p, _vp]),
+    ("zero3_load_shard", C.c_int, [_vp, C.c_int32, _c_i64_p, _vp, _vp, _vp, C.c_char_p, _vp]),
+    ("zero3_save_persistent", C.c_int, [_vp, C.c_int64, C.POINTER(PersistState), C.c_char_p, _vp]),
+    ("zero3_load_persistent", C.c_int, [_vp, _c_i64_p, C.POINTER(PersistState), C.c_char_p, _vp]),
+    ("zero3_save_16bit_weights", C.c_int, [_vp, _vp, _vp, C.c_char_p, _vp]),
     ("zero3_memory_bytes", C.c_int, [C.c_int32, C.c_double, C.c_int32, C.POINTER(C.c_double)]),
     ("zero3_comm_elems", C.c_int, [C.c_int32, C.c_double, C.c_int32, C.POINTER(C.c_double)]),
     ("zero3_sync", C.c_int, [_vp]),
@@ -226,6 +234,13 @@ def zero3_step(plan: Plan, hp, t, grads, grads_origin, master, m, v, sparam, ful
                                 _ps_ref(persist), flat_lo, flat_hi, stream), "zero3_step")
 
 
+def zero3_step_stage12(plan: Plan, hp, t, grads, grads_origin, master, m, v, params, flat_lo,
+                       flat_hi, stream=0):
+    _check(plan._lib.zero3_step_stage12(plan.handle, C.byref(hp), t, _ptrs(grads), grads_origin,
+                                        _ptrs(master), _ptrs(m), _ptrs(v), _ptrs(params), flat_lo,
+                                        flat_hi, stream), "zero3_step_stage12")
+
+
 def zero3_persistent_step(plan: Plan, hp, t, persist, stream=0):
     _check(plan._lib.zero3_persistent_step(plan.handle, C.byref(hp), t, _ps_ref(persist), stream),
            "zero3_persistent_step")
@@ -254,6 +269,39 @@ def zero3_submodule_status(plan: Plan, k) -> int:
 
 def zero3_submodule_wait(plan: Plan, k):
     _check(plan._lib.zero3_submodule_wait(plan.handle, k), "zero3_submodule_wait")
+
+
+def _path(path) -> bytes:
+    return os.fsencode(path)
+
+
+def zero3_save_shard(plan: Plan, rank, t, master, m, v, path, stream=0):
+    _check(plan._lib.zero3_save_shard(plan.handle, rank, t, master, m, v, _path(path), stream),
+           "zero3_save_shard")
+
+
+def zero3_load_shard(plan: Plan, rank, master, m, v, path, stream=0) -> int:
+    t = C.c_int64()
+    _check(plan._lib.zero3_load_shard(plan.handle, rank, C.byref(t), master, m, v, _path(path),
+                                      stream), "zero3_load_shard")
+    return t.value
+
+
+def zero3_save_persistent(plan: Plan, t, persist, path, stream=0):
+    _check(plan._lib.zero3_save_persistent(plan.handle, t, _ps_ref(persist), _path(path), stream),
+           "zero3_save_persistent")
+
+
+def zero3_load_persistent(plan: Plan, persist, path, stream=0) -> int:
+    t = C.c_int64()
+    _check(plan._lib.zero3_load_persistent(plan.handle, C.byref(t), _ps_ref(persist), _path(path),
+                                           stream), "zero3_load_persistent")
+    return t.value
+
+
+def zero3_save_16bit_weights(plan: Plan, full, persist_param, path, stream=0):
+    _check(plan._lib.zero3_save_16bit_weights(plan.handle, full or None, persist_param or None,
+                                              _path(path), stream), "zero3_save_16bit_weights")
 
 
 def zero3_memory_bytes(stage, psi, n_d) -> float:

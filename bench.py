@@ -55,6 +55,11 @@ def parse():
     ap.add_argument("--stage", type=int, choices=[2, 3], default=3,
                     help="3: ZeRO-3 step (default); 2: the ZeRO-1/2 step (full parameters on "
                          "every rank, no submodule gathers)")
+    ap.add_argument("--coordinator", action="store_true",
+                    help="measure the prefetching coordinator: forward/backward gathers "
+                         "interleaved with a GEMM per submodule, prefetch on vs off")
+    ap.add_argument("--tokens", type=int, default=4096,
+                    help="rows of the stand-in activation for --coordinator")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -318,6 +323,102 @@ def run_stage12(args):
     return 0
 
 
+def run_coordinator(args):
+    """Forward then backward over the submodules, each gathered through the
+    prefetching coordinator and consumed by bf16 GEMMs (one in forward, two
+    in backward) that stand in for the model's compute, then the fused
+    optimizer step.  Timed three ways on the same buffers: prefetch on,
+    prefetch off (every gather on demand), and the GEMMs alone (no gathers);
+    the difference off - on is the gather time the prefetch hides."""
+    import torch
+    from zero_sharded_optimizer_shard_gb300 import build as b
+    b.build_all(quiet=True)
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+    torch.cuda.set_device(0)
+    w = make_workload(args)
+    compute, prefetch = torch.cuda.Stream(), torch.cuda.Stream()
+    e = Emulation(w, stream=compute)
+    with torch.cuda.stream(compute):
+        e.init_params()
+        e.fill_grads(1)
+    plan = e.plan
+    n_sub = plan.info.n_submodules
+    sizes = [plan.submodule(k)[1] for k in range(n_sub)]
+    trace = list(range(n_sub)) + list(reversed(range(n_sub)))
+    arena_elems = 3 * max(sizes)
+    arena = torch.empty(arena_elems, dtype=torch.bfloat16, device="cuda")
+    width = 1024
+    X = torch.randn(args.tokens, width, dtype=torch.bfloat16, device="cuda")
+    Y = torch.empty(args.tokens, max(sizes) // width + 1, dtype=torch.bfloat16, device="cuda")
+    dX = torch.empty(args.tokens, width, dtype=torch.bfloat16, device="cuda")
+    Wfix = torch.randn(arena_elems, dtype=torch.bfloat16, device="cuda")
+
+    def gemms(buf, off, k, backward):
+        cols = sizes[k] // width
+        if cols == 0:
+            return
+        Wv = buf[off:off + cols * width].view(width, cols)
+        torch.matmul(X, Wv, out=Y[:, :cols])
+        if backward:
+            torch.matmul(Y[:, :cols], Wv.t(), out=dX)
+
+    def one_step(co, t):
+        for i, k in enumerate(trace):
+            if co is None:
+                with torch.cuda.stream(compute):
+                    gemms(Wfix, 0, k, i >= n_sub)
+                continue
+            ptr = co.fetch(k)
+            with torch.cuda.stream(compute):
+                gemms(arena, (ptr - arena.data_ptr()) // 2, k, i >= n_sub)
+            co.release(k)
+        e.step(t)
+        if co is not None:
+            co.next_step()
+
+    results = {}
+    t = 0
+    for mode, bucket in (("prefetch", w.bucket), ("on_demand", 0), ("gemm_only", None)):
+        co = None
+        if bucket is not None:
+            co = zero3.Coordinator(plan, trace, e.ptrs(e.sparam), e.pparam.data_ptr(),
+                                   arena.data_ptr(), arena_elems, prefetch_bucket_size=bucket,
+                                   max_live_parameters=arena_elems,
+                                   max_reuse_distance=10**9, compute_stream=compute.cuda_stream,
+                                   prefetch_stream=prefetch.cuda_stream)
+        for _ in range(args.warmup):
+            t += 1
+            one_step(co, t)
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(compute)
+        for _ in range(args.steps):
+            t += 1
+            one_step(co, t)
+        s1.record(compute)
+        torch.cuda.synchronize()
+        results[mode] = {"ms_per_step": s0.elapsed_time(s1) / args.steps}
+        if co is not None:
+            results[mode]["stats"] = co.stats()
+        del co
+    hidden = results["on_demand"]["ms_per_step"] - results["prefetch"]["ms_per_step"]
+    exposed = results["on_demand"]["ms_per_step"] - results["gemm_only"]["ms_per_step"]
+    print(json.dumps({
+        "metric": "ZeRO-3 forward/backward step with submodule gathers, prefetch on vs off",
+        "value": results["prefetch"]["ms_per_step"], "unit": "ms/step", "higher_is_better": False,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.workload][3], "tokens": args.tokens,
+                   "compute": f"bf16 GEMM [{args.tokens} x {width}] x [{width} x numel/{width}] "
+                              "per submodule (2 in backward)",
+                   "arena_elems": arena_elems, "prefetch_bucket_size": w.bucket},
+        "modes": results,
+        "gather_ms_hidden": hidden,
+        "gather_ms_exposed_without_prefetch": exposed,
+        "hidden_fraction": hidden / exposed if exposed > 0 else None}))
+    return 0
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -507,6 +608,8 @@ def main():
         return run_reference(args)
     if args.stage == 2:
         return run_stage12(args)
+    if args.coordinator:
+        return run_coordinator(args)
     return run_ours(args)
 
 

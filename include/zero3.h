@@ -286,6 +286,90 @@ zero3_status zero3_submodule_status(zero3_plan* plan, int32_t k, int32_t* status
 /* Blocks the host until submodule k's gather has finished; marks AVAILABLE. */
 zero3_status zero3_submodule_wait(zero3_plan* plan, int32_t k);
 
+/* ------------------------------------------------- prefetching coordinator
+ * Gathers the submodules that come next while the current one computes
+ * ([hotelren]: fetch_sub_module starts collecting later layers' parameters
+ * before the current layer has finished; [cnhsyj] section 3.2 and
+ * [hotelren], tuning list: stage3_prefetch_bucket_size,
+ * stage3_max_live_parameters, stage3_max_reuse_distance).
+ *  - Gathers run on prefetch_stream into a caller-owned arena (bf16,
+ *    arena_elems >= the largest submodule); the compute stream waits on a
+ *    submodule's ready event before its first use, so a fetch never blocks
+ *    the host.  Ranges of the arena are reused only after the compute stream
+ *    has passed the release of their previous contents.
+ *  - Order: `trace` (n_trace submodule ids) is the fetch order of one step;
+ *    with n_trace = 0 the order of the first step is recorded (no prefetch
+ *    during it) and used from the next step on.  A fetch that departs from
+ *    the order disables prefetching until the next step (counted in
+ *    trace_misses) and the new order is adopted.
+ *  - Budgets (elements): at most prefetch_bucket_size gathered ahead of use
+ *    (0 disables prefetching), at most max_live_parameters gathered at once;
+ *    a submodule whose next use comes within max_reuse_distance gathered
+ *    elements stays gathered after its release.  When the arena or the live
+ *    budget is exhausted, unreferenced copies are dropped, farthest next use
+ *    first; ZERO3_ENOMEM when only referenced copies remain.
+ *  - Status per submodule follows the ZeroParamStatus machine
+ *    (NOT_AVAILABLE, INFLIGHT, AVAILABLE).
+ *  - sparam (n_ranks device pointers) and persist_param are read at every
+ *    gather; their contents change only through the optimizer step, after
+ *    which the caller calls zero3_coordinator_next_step.
+ *  - compute_stream and prefetch_stream must differ; the coordinator records
+ *    events on both and never synchronises the host. */
+typedef struct zero3_coordinator zero3_coordinator;
+
+typedef struct zero3_prefetch_config {
+    int64_t prefetch_bucket_size;  /* stage3_prefetch_bucket_size */
+    int64_t max_live_parameters;   /* stage3_max_live_parameters */
+    int64_t max_reuse_distance;    /* stage3_max_reuse_distance */
+} zero3_prefetch_config;
+
+typedef struct zero3_coordinator_stats {
+    int64_t steps;           /* zero3_coordinator_next_step calls */
+    int64_t gathers;         /* gathers issued (ahead of use or on demand) */
+    int64_t prefetched;      /* gathers issued ahead of use */
+    int64_t prefetch_hits;   /* fetches served by a gather issued ahead */
+    int64_t reuse_hits;      /* fetches served by a copy kept after release */
+    int64_t evictions;       /* unreferenced copies dropped for room */
+    int64_t trace_misses;    /* fetches that departed from the order */
+    int64_t gathered_elems;
+    int64_t peak_live_elems;
+    int64_t live_elems;
+} zero3_coordinator_stats;
+
+/* EINVAL: NULL plan/cfg/out, negative sizes, equal streams, arena smaller
+ * than the largest submodule, max_live below it, a trace id out of range, a
+ * NULL or misaligned source shard or arena. */
+zero3_status zero3_coordinator_create(zero3_plan* plan, const int32_t* trace, int64_t n_trace,
+                                      const uint16_t* const* sparam,
+                                      const uint16_t* persist_param, uint16_t* arena,
+                                      int64_t arena_elems, const zero3_prefetch_config* cfg,
+                                      zero3_stream compute_stream, zero3_stream prefetch_stream,
+                                      zero3_coordinator** out);
+
+/* Takes a reference to submodule k's gathered parameters (layout as
+ * zero3_fetch_submodule) and issues the next prefetches.  *out points into
+ * the arena and is valid for work enqueued on compute_stream until the
+ * matching release. */
+zero3_status zero3_coordinator_fetch(zero3_coordinator* c, int32_t k, uint16_t** out);
+
+/* Drops a reference (ESTATE if k holds none). */
+zero3_status zero3_coordinator_release(zero3_coordinator* c, int32_t k);
+
+zero3_status zero3_coordinator_status(zero3_coordinator* c, int32_t k, int32_t* status);
+
+/* Call after the optimizer step has been enqueued on compute_stream: drops
+ * every gathered copy (they predate the update), orders later gathers after
+ * the step, adopts the recorded order if needed and prefetches the start of
+ * the next step.  ESTATE if a reference is still held. */
+zero3_status zero3_coordinator_next_step(zero3_coordinator* c);
+
+zero3_status zero3_coordinator_get_stats(const zero3_coordinator* c,
+                                         zero3_coordinator_stats* stats);
+
+/* Frees the coordinator's events; the arena stays the caller's.  Work already
+ * enqueued keeps running. */
+void zero3_coordinator_destroy(zero3_coordinator* c);
+
 /* ------------------------------------------------------------ checkpoints
  * Each partition is saved and restored by itself ([cnhsyj] section 4.3:
  * save_checkpoint / load_checkpoint write and read every partition), or the

@@ -266,3 +266,32 @@ def test_checkpoint_load_rejects_bad_files(lib, tmp_path):
                             None) == zero3.EINVAL
     assert zero3.raw_status("zero3_save_16bit_weights", p.handle, MISALIGNED, FAKE, b"x",
                             None) == zero3.EINVAL
+
+
+def test_coordinator_create_rejects_bad_arguments(lib):
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    p = _plan()
+    out = C.c_void_p()
+    big = p.submodule(1)[1]
+    cfg = zero3.PrefetchConfig(10**6, 10**6, 10**6)
+    P = zero3._ptrs
+    S1, S2 = 0x1000, 0x2000  # two distinct stream handles (never used: creation fails first)
+
+    def create(trace=(0, 1), sparam=(FAKE, FAKE), persist=FAKE, arena=FAKE, n=big, cfg_=cfg,
+               s1=S1, s2=S2):
+        tr = (C.c_int32 * max(len(trace), 1))(*trace)
+        return zero3.raw_status("zero3_coordinator_create", p.handle, tr, len(trace),
+                                P(list(sparam)) if sparam is not None else None, persist, arena,
+                                n, C.byref(cfg_) if cfg_ is not None else None, s1, s2,
+                                C.byref(out))
+    E = zero3.EINVAL
+    assert create(n=big - 1) == E                       # arena below the largest submodule
+    assert create(cfg_=zero3.PrefetchConfig(0, big - 1, 0)) == E  # live budget too small
+    assert create(cfg_=zero3.PrefetchConfig(-1, big, 0)) == E
+    assert create(cfg_=None) == E
+    assert create(s2=S1) == E                           # same stream twice
+    assert create(trace=(0, 2)) == E                    # unknown submodule
+    assert create(sparam=(FAKE, 0)) == E                # missing shard
+    assert create(sparam=None) == E
+    assert create(arena=MISALIGNED) == E
+    assert create(persist=0) == E                       # submodule 0 holds a persistent tensor

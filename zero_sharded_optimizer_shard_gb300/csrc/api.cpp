@@ -152,6 +152,73 @@ zero3_status persistent_launch(const zero3_plan* p, const z3::Scalars& sc,
 
 }  // namespace
 
+namespace z3 {
+
+zero3_status check_gather_sources(const zero3_plan* p, int32_t k, const uint16_t* const* sparam,
+                                  const uint16_t* persist_param, const uint16_t* out) {
+    if (p->sub_numel[k] > 0 && (!out || !aligned16(out))) return ZERO3_EINVAL;
+    for (int64_t t : p->sub_tensors[k]) {
+        if (p->numel[t] == 0) continue;
+        if (p->persistent[t]) {
+            if (!persist_param || !aligned16(persist_param)) return ZERO3_EINVAL;
+        } else {
+            if (!sparam) return ZERO3_EINVAL;
+            for (int64_t s = p->seg_begin[t]; s < p->seg_begin[t + 1]; ++s) {
+                const uint16_t* src = sparam[p->segs[s].rank];
+                if (!src || !aligned16(src)) return ZERO3_EINVAL;
+            }
+        }
+    }
+    return ZERO3_OK;
+}
+
+zero3_status gather_submodule(const zero3_plan* p, int32_t k, const uint16_t* const* sparam,
+                              const uint16_t* persist_param, uint16_t* out, cudaStream_t stream) {
+    GatherArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.out = out;
+    int64_t running = 0;
+    auto flush = [&]() -> zero3_status {
+        zero3_status st = cuda_status(launch_gather(a, stream));
+        a.n_segs = 0;
+        a.total_chunks = 0;
+        return st;
+    };
+    auto push = [&](const uint16_t* src, int64_t dst_off, int64_t len) -> zero3_status {
+        if (len <= 0) return ZERO3_OK;
+        if (a.n_segs == kMaxGatherSegs) {
+            zero3_status st = flush();
+            if (st != ZERO3_OK) return st;
+        }
+        GatherSeg& g = a.seg[a.n_segs++];
+        g.src = src;
+        g.dst_off = dst_off;
+        g.len = len;
+        g.chunk0 = a.total_chunks;
+        const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
+        g.vec = ((sa - 2u * static_cast<uintptr_t>(dst_off)) % 16u == 0) ? 1 : 0;
+        a.total_chunks += ((dst_off + len) - (dst_off & ~static_cast<int64_t>(7)) + 7) / 8;
+        return ZERO3_OK;
+    };
+    for (int64_t t : p->sub_tensors[k]) {
+        zero3_status st = ZERO3_OK;
+        if (p->persistent[t]) {
+            st = push(persist_param + p->offset[t], running, p->numel[t]);
+        } else {
+            for (int64_t s = p->seg_begin[t]; s < p->seg_begin[t + 1] && st == ZERO3_OK; ++s) {
+                const zero3_segment& sg = p->segs[s];
+                st = push(sparam[sg.rank] + sg.shard_off, running + sg.tensor_off, sg.len);
+            }
+        }
+        if (st != ZERO3_OK) return st;
+        running += p->numel[t];
+    }
+    if (a.n_segs > 0) return flush();
+    return ZERO3_OK;
+}
+
+}  // namespace z3
+
 extern "C" {
 
 zero3_status zero3_reduce_scatter(const zero3_plan* p, const uint16_t* const* grads,
@@ -327,70 +394,16 @@ zero3_status zero3_fetch_submodule(zero3_plan* p, int32_t k, const uint16_t* con
         p->refs[k] += 1;
         return ZERO3_OK;
     }
-    const int64_t total = p->sub_numel[k];
-    if (total > 0 && (!out || !aligned16(out))) return ZERO3_EINVAL;
-    // Validate every source first so that an error launches nothing.
-    for (int64_t t : p->sub_tensors[k]) {
-        if (p->numel[t] == 0) continue;
-        if (p->persistent[t]) {
-            if (!persist_param || !aligned16(persist_param)) return ZERO3_EINVAL;
-        } else {
-            if (!sparam) return ZERO3_EINVAL;
-            for (int64_t s = p->seg_begin[t]; s < p->seg_begin[t + 1]; ++s) {
-                const uint16_t* src = sparam[p->segs[s].rank];
-                if (!src || !aligned16(src)) return ZERO3_EINVAL;
-            }
-        }
-    }
+    zero3_status st = z3::check_gather_sources(p, k, sparam, persist_param, out);
+    if (st != ZERO3_OK) return st;
     if (!p->events[k]) {
         if (cudaEventCreateWithFlags(&p->events[k], cudaEventDisableTiming) != cudaSuccess) {
             p->events[k] = nullptr;
             return ZERO3_ECUDA;
         }
     }
-    z3::GatherArgs a;
-    std::memset(&a, 0, sizeof(a));
-    a.out = out;
-    int64_t running = 0;
-    auto flush = [&]() -> zero3_status {
-        zero3_status st = cuda_status(z3::launch_gather(a, stream));
-        a.n_segs = 0;
-        a.total_chunks = 0;
-        return st;
-    };
-    auto push = [&](const uint16_t* src, int64_t dst_off, int64_t len) -> zero3_status {
-        if (len <= 0) return ZERO3_OK;
-        if (a.n_segs == z3::kMaxGatherSegs) {
-            zero3_status st = flush();
-            if (st != ZERO3_OK) return st;
-        }
-        z3::GatherSeg& g = a.seg[a.n_segs++];
-        g.src = src;
-        g.dst_off = dst_off;
-        g.len = len;
-        g.chunk0 = a.total_chunks;
-        const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
-        g.vec = ((sa - 2u * static_cast<uintptr_t>(dst_off)) % 16u == 0) ? 1 : 0;
-        a.total_chunks += ((dst_off + len) - (dst_off & ~static_cast<int64_t>(7)) + 7) / 8;
-        return ZERO3_OK;
-    };
-    for (int64_t t : p->sub_tensors[k]) {
-        zero3_status st = ZERO3_OK;
-        if (p->persistent[t]) {
-            st = push(persist_param + p->offset[t], running, p->numel[t]);
-        } else {
-            for (int64_t s = p->seg_begin[t]; s < p->seg_begin[t + 1] && st == ZERO3_OK; ++s) {
-                const zero3_segment& sg = p->segs[s];
-                st = push(sparam[sg.rank] + sg.shard_off, running + sg.tensor_off, sg.len);
-            }
-        }
-        if (st != ZERO3_OK) return st;
-        running += p->numel[t];
-    }
-    if (a.n_segs > 0) {
-        zero3_status st = flush();
-        if (st != ZERO3_OK) return st;
-    }
+    st = z3::gather_submodule(p, k, sparam, persist_param, out, stream);
+    if (st != ZERO3_OK) return st;
     if (cudaEventRecord(p->events[k], stream) != cudaSuccess) return ZERO3_ECUDA;
     p->status[k] = ZERO3_INFLIGHT;
     p->refs[k] = 1;

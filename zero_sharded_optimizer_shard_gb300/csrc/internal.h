@@ -99,6 +99,14 @@ struct GatherArgs {
 };
 
 cudaError_t launch_stream(int mode, const StreamArgs& a, cudaStream_t stream);
+
+// Submodule gather shared by zero3_fetch_submodule and the prefetch
+// coordinator: validation of the sources, and the launches (one per 64
+// pieces) writing submodule k's tensors contiguously into out.
+zero3_status check_gather_sources(const zero3_plan* p, int32_t k, const uint16_t* const* sparam,
+                                  const uint16_t* persist_param, const uint16_t* out);
+zero3_status gather_submodule(const zero3_plan* p, int32_t k, const uint16_t* const* sparam,
+                              const uint16_t* persist_param, uint16_t* out, cudaStream_t stream);
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream);
 
 }  // namespace z3

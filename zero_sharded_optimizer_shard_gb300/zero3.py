@@ -56,6 +56,20 @@ class PersistState(C.Structure):
                 ("param", _vp)]
 
 
+class PrefetchConfig(C.Structure):
+    _fields_ = [("prefetch_bucket_size", C.c_int64), ("max_live_parameters", C.c_int64),
+                ("max_reuse_distance", C.c_int64)]
+
+
+class CoordinatorStats(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("steps", "gathers", "prefetched", "prefetch_hits",
+                                          "reuse_hits", "evictions", "trace_misses",
+                                          "gathered_elems", "peak_live_elems", "live_elems")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
 class Zero3Error(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -94,6 +108,15 @@ _SIGS = [
     ("zero3_release_submodule", C.c_int, [_vp, C.c_int32]),
     ("zero3_submodule_status", C.c_int, [_vp, C.c_int32, _c_i32_p]),
     ("zero3_submodule_wait", C.c_int, [_vp, C.c_int32]),
+    ("zero3_coordinator_create", C.c_int, [_vp, _c_i32_p, C.c_int64, C.POINTER(_vp), _vp, _vp,
+                                           C.c_int64, C.POINTER(PrefetchConfig), _vp, _vp,
+                                           C.POINTER(_vp)]),
+    ("zero3_coordinator_fetch", C.c_int, [_vp, C.c_int32, C.POINTER(_vp)]),
+    ("zero3_coordinator_release", C.c_int, [_vp, C.c_int32]),
+    ("zero3_coordinator_status", C.c_int, [_vp, C.c_int32, _c_i32_p]),
+    ("zero3_coordinator_next_step", C.c_int, [_vp]),
+    ("zero3_coordinator_get_stats", C.c_int, [_vp, C.POINTER(CoordinatorStats)]),
+    ("zero3_coordinator_destroy", None, [_vp]),
     ("zero3_save_shard", C.c_int, [_vp, C.c_int32, C.c_int64, _vp, _vp, _vp, C.c_char_p, _vp]),
     ("zero3_load_shard", C.c_int, [_vp, C.c_int32, _c_i64_p, _vp, _vp, _vp, C.c_char_p, _vp]),
     ("zero3_save_persistent", C.c_int, [_vp, C.c_int64, C.POINTER(PersistState), C.c_char_p, _vp]),
@@ -269,6 +292,57 @@ def zero3_submodule_status(plan: Plan, k) -> int:
 
 def zero3_submodule_wait(plan: Plan, k):
     _check(plan._lib.zero3_submodule_wait(plan.handle, k), "zero3_submodule_wait")
+
+
+class Coordinator:
+    """Owner of a zero3_coordinator* (prefetching gathers into an arena)."""
+
+    def __init__(self, plan: Plan, trace, sparam, persist_param, arena, arena_elems,
+                 prefetch_bucket_size=500_000_000, max_live_parameters=1_000_000_000,
+                 max_reuse_distance=1_000_000_000, compute_stream=0, prefetch_stream=0):
+        lib = plan._lib
+        self._lib = lib
+        self.plan = plan  # keeps the plan alive
+        tr = list(trace or [])
+        ta = (C.c_int32 * max(len(tr), 1))(*tr)
+        self.cfg = PrefetchConfig(prefetch_bucket_size, max_live_parameters, max_reuse_distance)
+        out = _vp()
+        _check(lib.zero3_coordinator_create(plan.handle, ta if tr else None, len(tr),
+                                            _ptrs(sparam), persist_param or None, arena or None,
+                                            arena_elems, C.byref(self.cfg), compute_stream,
+                                            prefetch_stream, C.byref(out)),
+               "zero3_coordinator_create")
+        self.handle = out
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h:
+            self._lib.zero3_coordinator_destroy(h)
+            self.handle = None
+
+    def fetch(self, k: int) -> int:
+        p = _vp()
+        _check(self._lib.zero3_coordinator_fetch(self.handle, k, C.byref(p)),
+               "zero3_coordinator_fetch")
+        return p.value or 0
+
+    def release(self, k: int) -> None:
+        _check(self._lib.zero3_coordinator_release(self.handle, k), "zero3_coordinator_release")
+
+    def status(self, k: int) -> int:
+        s = C.c_int32()
+        _check(self._lib.zero3_coordinator_status(self.handle, k, C.byref(s)),
+               "zero3_coordinator_status")
+        return s.value
+
+    def next_step(self) -> None:
+        _check(self._lib.zero3_coordinator_next_step(self.handle), "zero3_coordinator_next_step")
+
+    def stats(self) -> dict:
+        st = CoordinatorStats()
+        _check(self._lib.zero3_coordinator_get_stats(self.handle, C.byref(st)),
+               "zero3_coordinator_get_stats")
+        return st.as_dict()
 
 
 def _path(path) -> bytes:

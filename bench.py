@@ -60,6 +60,9 @@ def parse():
                          "interleaved with a GEMM per submodule, prefetch on vs off")
     ap.add_argument("--tokens", type=int, default=4096,
                     help="rows of the stand-in activation for --coordinator")
+    ap.add_argument("--qwz", action="store_true",
+                    help="ZeRO++ qwZ: the fused step emits int8 codes + block scales and the "
+                         "all-gather dequantizes them into the full buffer")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -419,6 +422,87 @@ def run_coordinator(args):
     return 0
 
 
+def run_qwz(args):
+    """The qwZ step: fused reduce-scatter + AdamW + bf16 shard + int8 block
+    quantization, then the dequantizing all-gather into the full buffer."""
+    import torch
+    from zero_sharded_optimizer_shard_gb300 import build as b
+    b.build_all(quiet=True)
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+    torch.cuda.set_device(0)
+    fac, state_ranks, bucketed, desc = WORKLOADS[args.workload]
+    if state_ranks is not None:
+        raise SystemExit("--qwz needs a full emulation workload")
+    w = make_workload(args)
+    stream = torch.cuda.Stream()
+    e = Emulation(w, stream=stream)
+    nb = -(-e.S // 256)
+    with torch.cuda.stream(stream):
+        e.init_params()
+        e.fill_grads(1)
+        codes = [torch.empty(e.S, dtype=torch.int8, device="cuda") for _ in range(e.nd)]
+        scales = [torch.empty(nb, dtype=torch.float32, device="cuda") for _ in range(e.nd)]
+    torch.cuda.synchronize()
+    cp, sp = e.ptrs(codes), e.ptrs(scales)
+    lo, hi = e.chunks[0]
+    ev = []
+
+    def step(t, timed):
+        a0, a1, a2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a0.record(stream)
+        zero3.zero3_step_qwz(e.plan, e.hp, t, e.ptrs(e.grads[0]), lo, e.ptrs(e.master), e.ptrs(e.m),
+                             e.ptrs(e.v), e.ptrs(e.sparam), cp, sp, None, lo, hi, e.sid)
+        a1.record(stream)
+        zero3.zero3_allgather_qwz(e.plan, cp, sp, e.full.data_ptr(), lo, hi, e.sid)
+        a2.record(stream)
+        zero3.zero3_persistent_step(e.plan, e.hp, t, e.persist, e.sid)
+        if timed:
+            ev.append((a0, a1, a2))
+
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        step(t, False)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.5)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    tw0 = time.time()
+    s0.record(stream)
+    for _ in range(args.steps):
+        t += 1
+        step(t, True)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    tw1 = time.time()
+    clk = clocks.stop(tw0, tw1)
+    ms = s0.elapsed_time(s1) / args.steps
+    fused_ms = statistics.mean(a.elapsed_time(b_) for a, b_, _ in ev)
+    gather_ms = statistics.mean(b_.elapsed_time(c) for _, b_, c in ev)
+    n = hi - lo
+    fused_bytes = n * (2 * w.n_ranks + 24 + 2 + 1) + e.nd * nb * 4
+    gather_bytes = n * (1 + 2) + e.nd * nb * 4
+    peak, peak_kind = peaks()
+    ach = fused_bytes / (fused_ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": METRIC, "value": w.psi / (ms / 1e3), "unit": "params/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": desc + ", qwZ int8 all-gather (block 256)", "name": args.workload,
+                   "n_ranks": w.n_ranks, "params": w.psi},
+        "fused_qwz": {"ms_per_launch": fused_ms, "bytes_per_launch": fused_bytes,
+                      "gbs": ach, "frac": ach / peak},
+        "allgather_qwz": {"ms_per_launch": gather_ms, "bytes_per_launch": gather_bytes,
+                          "gbs": gather_bytes / (gather_ms / 1e3) / 1e9},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                     "frac": ach / peak, "peak_kind": peak_kind, "traffic": None,
+                     "kernel": "stream_kernel<kFusedQ, N_d> (zero3_step_qwz)"},
+        "gpu_launches": 3 * args.steps, "clocks": clk, "cpu_baseline": None, "e2e": None}))
+    return 0
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -610,6 +694,8 @@ def main():
         return run_stage12(args)
     if args.coordinator:
         return run_coordinator(args)
+    if args.qwz:
+        return run_qwz(args)
     return run_ours(args)
 
 

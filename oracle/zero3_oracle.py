@@ -20,6 +20,8 @@ What it computes, with the passages each part follows:
 * replicated_step -- the ZeRO-1/2 step: every rank keeps full parameters.
 * fetch_submodule -- gather a submodule's shards into one contiguous tensor.
 * gather_16bit_weights -- every tensor complete, in list order (save).
+* qwz_quantize, qwz_dequantize, qwz_allgather -- the int8 quantized
+                   parameter all-gather of ZeRO++ (qwZ).
 * memory_bytes, comm_elems, ring_send_bytes -- the model-state and
                    communication accounting.
 
@@ -438,6 +440,53 @@ def ddp_step(plan: Plan, hp: dict, t: int, grads: Sequence[np.ndarray], st: DDPS
         st.param[d] = cast_bf16(p)
     for d in range(1, plan.n_ranks):
         assert np.array_equal(st.master[d].view(np.uint32), st.master[0].view(np.uint32))
+
+
+# --------------------------------------------------------------------------
+# quantized weight all-gather (ZeRO++ qwZ)
+# --------------------------------------------------------------------------
+QWZ_BLOCK = 256
+
+
+def qwz_quantize(param_bf16: np.ndarray, block: int = QWZ_BLOCK):
+    """Quantize one rank's 2-byte parameter shard for the all-gather.
+
+    ZeRO++'s qwZ sends the weights of the parameter all-gather quantized to
+    int8 (or int4) to cut the communicated volume (ZeRO concept page,
+    section ZeRO++).  The pages give no block size or scale format; reading
+    taken: symmetric int8, one binary32 scale per `block` consecutive
+    elements of the shard (the last block may be shorter):
+        absmax = max |x| over the block (x = f32(bf16 param), exact)
+        scale  = absmax / 127                      (one binary32 division)
+        inv    = 127 / absmax, or 0 when absmax = 0 (one binary32 division)
+        code   = round_half_even(x * inv)          (one binary32 product)
+    Returns (int8 codes, binary32 scales)."""
+    x = bf16_to_f32(param_bf16)
+    n = x.size
+    nb = -(-n // block)
+    codes = np.zeros(n, np.int8)
+    scales = np.zeros(nb, np.float32)
+    for b in range(nb):
+        xb = x[b * block:(b + 1) * block]
+        amax = np.max(np.abs(xb)) if xb.size else F32(0)
+        scales[b] = F32(amax) / F32(127.0)
+        inv = (F32(127.0) / F32(amax)) if amax > 0 else F32(0.0)
+        codes[b * block:(b + 1) * block] = np.clip(np.rint(xb * inv), -127, 127).astype(np.int8)
+    return codes, scales
+
+
+def qwz_dequantize(codes: np.ndarray, scales: np.ndarray, block: int = QWZ_BLOCK) -> np.ndarray:
+    """Receiver side: bf16(code * scale), one binary32 product rounded once
+    to bf16 (nearest even)."""
+    s = np.repeat(scales, block)[:codes.size]
+    return bf16_rne(codes.astype(np.float32) * s)
+
+
+def qwz_allgather(plan: Plan, codes: Sequence[np.ndarray], scales: Sequence[np.ndarray]) -> np.ndarray:
+    """All-gather of the quantized shards: rank r's dequantized shard lands
+    at [r*S, (r+1)*S) of the full buffer."""
+    return np.concatenate([qwz_dequantize(c, s) for c, s in zip(codes, scales)]) \
+        if plan.n_ranks else np.zeros(0, np.uint16)
 
 
 # --------------------------------------------------------------------------

@@ -1,0 +1,106 @@
+"""qwZ (quantized parameter all-gather) through the C ABI against the oracle:
+the fused step's states and shards, its int8 codes and block scales, and
+the dequantizing all-gather, bit for bit."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle as O  # noqa: E402
+from tests._oracle_runs import bits, f32, host_grads, host_master, u16  # noqa: E402
+from zero_sharded_optimizer_shard_gb300 import workloads as W  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def wire(e):
+    nb = -(-e.S // 256)
+    codes = [torch.zeros(max(e.S, 16), dtype=torch.int8, device="cuda") for _ in range(e.nd)]
+    scales = [torch.zeros(max(nb, 4), dtype=torch.float32, device="cuda") for _ in range(e.nd)]
+    return codes, scales
+
+
+def i8(t):
+    return t.detach().cpu().numpy().view(np.int8)
+
+
+@pytest.mark.parametrize("wname", ["mini2", "mini3", "mini8", "ragged7"])
+def test_qwz_step_and_allgather_match_oracle(wname):
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+    w = {"mini2": lambda: W.mini_gpt(2), "mini3": lambda: W.mini_gpt(3),
+         "mini8": lambda: W.mini_gpt(8), "ragged7": lambda: W.ragged_small(7)}[wname]()
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    e = Emulation(w)
+    e.init_params()
+    codes, scales = wire(e)
+    mf, mp = host_master(w, plan)
+    st, full, _ = O.init_state(plan, mf, mp)
+    for t in range(1, 4):
+        e.fill_grads(t)
+        zero3.zero3_step_qwz(e.plan, e.hp, t, e.ptrs(e.grads[0]), 0, e.ptrs(e.master), e.ptrs(e.m),
+                             e.ptrs(e.v), e.ptrs(e.sparam), e.ptrs(codes), e.ptrs(scales), None,
+                             0, e.psi_pad, e.sid)
+        zero3.zero3_allgather_qwz(e.plan, e.ptrs(codes), e.ptrs(scales), e.full.data_ptr(), 0,
+                                  e.psi_pad, e.sid)
+        O.sharded_step(plan, w.hparams, t, host_grads(w, plan, t), st, full)
+    torch.cuda.synchronize()
+    q = [O.qwz_quantize(st.sparam[r]) for r in range(w.n_ranks)]
+    for r in range(w.n_ranks):
+        assert np.array_equal(bits(f32(e.master[r])), bits(st.master[r]))
+        assert np.array_equal(u16(e.sparam[r]), st.sparam[r])
+        assert np.array_equal(i8(codes[r])[:e.S], q[r][0]), f"codes rank {r}"
+        assert np.array_equal(bits(f32(scales[r])[:q[r][1].size]), bits(q[r][1])), f"scales {r}"
+    want = O.qwz_allgather(plan, [c for c, _ in q], [s for _, s in q])
+    assert np.array_equal(u16(e.full), want)
+
+
+def test_quantize_shards_and_partial_ranges():
+    """Standalone quantization == oracle; a block-aligned sub-range touches
+    only its blocks; a range that cuts a block is rejected; the dequantizing
+    gather accepts any range."""
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+    w = W.mini_gpt(3)
+    e = Emulation(w)
+    e.init_params()
+    codes, scales = wire(e)
+    S = e.S
+    zero3.zero3_quantize_shards(e.plan, e.ptrs(e.sparam), e.ptrs(codes), e.ptrs(scales), 0,
+                                e.psi_pad, e.sid)
+    torch.cuda.synchronize()
+    for r in range(3):
+        c, s = O.qwz_quantize(u16(e.sparam[r]))
+        assert np.array_equal(i8(codes[r])[:S], c)
+        assert np.array_equal(bits(f32(scales[r])[:s.size]), bits(s))
+    # sub-range: rank 1's blocks 2..5 only
+    for x in codes:
+        x.zero_()
+    zero3.zero3_quantize_shards(e.plan, e.ptrs(e.sparam), e.ptrs(codes), e.ptrs(scales),
+                                S + 512, S + 1536, e.sid)
+    torch.cuda.synchronize()
+    c1, _ = O.qwz_quantize(u16(e.sparam[1]))
+    got = i8(codes[1])
+    assert np.array_equal(got[512:1536], c1[512:1536])
+    assert not got[:512].any() and not got[1536:S].any() and not i8(codes[0]).any()
+    for bad in [(S + 100, S + 1536), (S + 512, S + 1000)]:
+        with pytest.raises(zero3.Zero3Error) as exc:
+            zero3.zero3_quantize_shards(e.plan, e.ptrs(e.sparam), e.ptrs(codes), e.ptrs(scales),
+                                        *bad, e.sid)
+        assert exc.value.status == zero3.EINVAL
+    # dequantize an odd range only (codes of every shard quantized again first)
+    zero3.zero3_quantize_shards(e.plan, e.ptrs(e.sparam), e.ptrs(codes), e.ptrs(scales), 0,
+                                e.psi_pad, e.sid)
+    e.full.zero_()
+    lo, hi = S - 13, 2 * S + 7
+    zero3.zero3_allgather_qwz(e.plan, e.ptrs(codes), e.ptrs(scales), e.full.data_ptr(), lo, hi,
+                              e.sid)
+    torch.cuda.synchronize()
+    got = u16(e.full)
+    assert not got[:lo].any() and not got[hi:].any()
+    c0, s0 = O.qwz_quantize(u16(e.sparam[0]))
+    c1, s1 = O.qwz_quantize(u16(e.sparam[1]))
+    c2, s2 = O.qwz_quantize(u16(e.sparam[2]))
+    assert np.array_equal(got[lo:S], O.qwz_dequantize(c0, s0)[lo:S])
+    assert np.array_equal(got[S:2 * S], O.qwz_dequantize(c1, s1))
+    assert np.array_equal(got[2 * S:hi], O.qwz_dequantize(c2, s2)[:hi - 2 * S])

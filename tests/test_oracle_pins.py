@@ -420,3 +420,47 @@ def test_state_machine():
     assert sm.status[0] == O.NOT_AVAILABLE
     with pytest.raises(RuntimeError):
         sm.release(1)
+
+
+# ---------------------------------------------------------------- qwZ quantized all-gather
+def test_qwz_hand_example():
+    g = golden("qwz_block_example.json")
+    codes, scales = O.qwz_quantize(bf16(g["x"]), block=g["block"])
+    assert list(codes) == g["codes"]
+    assert scales[0] == np.float32(g["absmax"]) / np.float32(127)
+    deq = O.bf16_to_f32(O.qwz_dequantize(codes, scales, block=g["block"]))
+    assert list(map(float, deq)) == g["dequant"]
+
+
+def test_qwz_error_bound_and_extremes():
+    """Per element |dequant - x| <= scale/2 (rounding of the code) plus the
+    binary32 product and the bf16 rounding of the result; the block's absmax
+    element maps to +-127; an all-zero block gives zero codes and scale."""
+    rng = np.random.default_rng(21)
+    x16 = bf16((rng.standard_normal(10_000) * 0.02).astype(np.float32))
+    x16[256:512] = 0
+    codes, scales = O.qwz_quantize(x16)
+    x = O.bf16_to_f32(x16).astype(np.float64)
+    y = O.bf16_to_f32(O.qwz_dequantize(codes, scales)).astype(np.float64)
+    s = np.repeat(scales.astype(np.float64), 256)[:x.size]
+    bound = s / 2 * (1 + 1e-6) + np.abs(x) * 2.0 ** -8 + 1e-45
+    assert np.all(np.abs(y - x) <= bound)
+    assert np.all(np.abs(codes.astype(int)) <= 127)
+    for b in range(scales.size):
+        blk = np.abs(x[b * 256:(b + 1) * 256])
+        if blk.max() > 0:
+            assert np.abs(codes[b * 256:(b + 1) * 256]).max() == 127
+        else:
+            assert scales[b] == 0 and not codes[b * 256:(b + 1) * 256].any()
+    assert scales.size == -(-10_000 // 256)  # last block partial
+
+
+def test_qwz_allgather_layout():
+    plan = O.partition([1000, 700], None, 3, threshold=0)
+    rng = np.random.default_rng(3)
+    shards = [bf16(rng.standard_normal(plan.shard_len).astype(np.float32)) for _ in range(3)]
+    q = [O.qwz_quantize(s) for s in shards]
+    full = O.qwz_allgather(plan, [c for c, _ in q], [s for _, s in q])
+    S = plan.shard_len
+    for r in range(3):
+        assert np.array_equal(full[r * S:(r + 1) * S], O.qwz_dequantize(*q[r]))

@@ -42,12 +42,16 @@ void rank_range(const zero3_plan* p, int r, int64_t lo, int64_t hi, int64_t* a, 
     *b = (hi < s1 ? hi : s1) - s0;
 }
 
-// Appends a span and advances the chunk counter.
-void add_span(StreamArgs& a, Span s) {
+// Appends a span and advances the chunk counter.  With warp_blocks, the
+// span's chunks start on a multiple of 32 so that each warp covers exactly
+// one 256-element qwZ block (the span then starts on a block boundary).
+void add_span(StreamArgs& a, Span s, bool warp_blocks = false) {
     const int64_t first = s.lo & ~static_cast<int64_t>(7);
+    if (warp_blocks) a.total_chunks = (a.total_chunks + 31) / 32 * 32;
     s.chunk0 = a.total_chunks;
     a.span[a.n_spans++] = s;
     a.total_chunks += (s.hi - first + 7) / 8;
+    if (warp_blocks) a.total_chunks = (a.total_chunks + 31) / 32 * 32;
 }
 
 struct RankPtrs {
@@ -61,7 +65,10 @@ struct RankPtrs {
     int out_elem = 2;                  // bytes per element of out
     int in_elem = 0;                   // bytes per element of in (0: unused)
     uint16_t* full = nullptr;
+    int8_t* const* codes = nullptr;    // qwZ codes per rank
+    float* const* scales = nullptr;    // qwZ scales per rank
     bool need_state = false;
+    bool warp_blocks = false;          // quantizing launch: one warp per 256-element block
 };
 
 // Builds the launch description of one mode over flat [lo, hi).  Validates
@@ -110,8 +117,19 @@ zero3_status build_args(const zero3_plan* p, int mode, const RankPtrs& rp, int64
             s.in = rp.in[r];
             if (!s.in || !aligned16(s.in)) return ZERO3_EINVAL;
         }
+        if (rp.codes) {
+            s.codes = rp.codes[r];
+            s.scales = rp.scales ? rp.scales[r] : nullptr;
+            if (!s.codes || !aligned16(s.codes) || !s.scales || !aligned16(s.scales))
+                return ZERO3_EINVAL;
+        }
+        if (rp.warp_blocks) {
+            // a quantizing launch covers whole blocks of each shard
+            if (la % z3::kQwzBlock != 0 || (lb % z3::kQwzBlock != 0 && lb != p->S))
+                return ZERO3_EINVAL;
+        }
         s.vec = vec ? 1 : 0;
-        add_span(a, s);
+        add_span(a, s, rp.warp_blocks);
     }
     return ZERO3_OK;
 }
@@ -336,6 +354,72 @@ zero3_status zero3_step_stage12(const zero3_plan* p, const zero3_adamw_hparams* 
     if (st != ZERO3_OK) return st;
     for (int q = 0; q < p->n_ranks; ++q) a.reps[q] = params[q];
     return cuda_status(z3::launch_stream(z3::kFusedRep, a, stream));
+}
+
+zero3_status zero3_step_qwz(const zero3_plan* p, const zero3_adamw_hparams* hp, int64_t t,
+                            const uint16_t* const* grads, int64_t grads_origin,
+                            float* const* master, float* const* m, float* const* v,
+                            uint16_t* const* sparam, int8_t* const* codes,
+                            float* const* scales, const zero3_persist_state* persist,
+                            int64_t lo, int64_t hi, zero3_stream stream) {
+    if (!p || !range_ok(p, lo, hi) || !hparams_ok(hp, t) || grads_origin > lo)
+        return ZERO3_EINVAL;
+    const z3::Scalars sc = step_scalars(p, hp, t);
+    if (lo < hi) {
+        if (!grads_ok(p, grads) || !sparam || !codes || !scales) return ZERO3_EINVAL;
+        RankPtrs rp;
+        rp.grads = grads;
+        rp.grads_origin = grads_origin;
+        rp.master = master;
+        rp.m = m;
+        rp.v = v;
+        rp.need_state = true;
+        rp.out = reinterpret_cast<void* const*>(sparam);
+        rp.codes = codes;
+        rp.scales = scales;
+        rp.warp_blocks = true;
+        StreamArgs a;
+        zero3_status st = build_args(p, z3::kFusedQ, rp, lo, hi, &sc, 0, a);
+        if (st != ZERO3_OK) return st;
+        if (persist && !persist_ok(p, persist)) return ZERO3_EINVAL;
+        st = cuda_status(z3::launch_stream(z3::kFusedQ, a, stream));
+        if (st != ZERO3_OK) return st;
+    }
+    if (persist) return persistent_launch(p, sc, persist, stream);
+    return ZERO3_OK;
+}
+
+zero3_status zero3_quantize_shards(const zero3_plan* p, const uint16_t* const* sparam,
+                                   int8_t* const* codes, float* const* scales, int64_t lo,
+                                   int64_t hi, zero3_stream stream) {
+    if (!p || !range_ok(p, lo, hi)) return ZERO3_EINVAL;
+    if (lo == hi) return ZERO3_OK;
+    if (!sparam || !codes || !scales) return ZERO3_EINVAL;
+    RankPtrs rp;
+    rp.in = reinterpret_cast<const void* const*>(sparam);
+    rp.codes = codes;
+    rp.scales = scales;
+    rp.warp_blocks = true;
+    StreamArgs a;
+    zero3_status st = build_args(p, z3::kQuant, rp, lo, hi, nullptr, 0, a);
+    if (st != ZERO3_OK) return st;
+    return cuda_status(z3::launch_stream(z3::kQuant, a, stream));
+}
+
+zero3_status zero3_allgather_qwz(const zero3_plan* p, const int8_t* const* codes,
+                                 const float* const* scales, uint16_t* full, int64_t lo,
+                                 int64_t hi, zero3_stream stream) {
+    if (!p || !range_ok(p, lo, hi)) return ZERO3_EINVAL;
+    if (lo == hi) return ZERO3_OK;
+    if (!codes || !scales || !full || !aligned16(full)) return ZERO3_EINVAL;
+    RankPtrs rp;
+    rp.full = full;
+    rp.codes = const_cast<int8_t* const*>(codes);
+    rp.scales = const_cast<float* const*>(scales);
+    StreamArgs a;
+    zero3_status st = build_args(p, z3::kDequant, rp, lo, hi, nullptr, 0, a);
+    if (st != ZERO3_OK) return st;
+    return cuda_status(z3::launch_stream(z3::kDequant, a, stream));
 }
 
 zero3_status zero3_persistent_step(const zero3_plan* p, const zero3_adamw_hparams* hp, int64_t t,

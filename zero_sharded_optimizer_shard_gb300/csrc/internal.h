@@ -48,7 +48,13 @@ enum Mode : int {
     kGather = 3,   // sparam -> full
     kCast = 4,     // master -> sparam (+ full)
     kFusedRep = 5, // grads -> reduce -> AdamW -> every rank's full copy (ZeRO-1/2)
+    kFusedQ = 6,   // grads -> reduce -> AdamW -> sparam + int8 codes/scales (qwZ)
+    kQuant = 7,    // sparam -> int8 codes/scales (qwZ)
+    kDequant = 8,  // int8 codes/scales -> full (qwZ all-gather)
 };
+
+// qwZ block: one warp's 32 chunks of 8 elements.
+constexpr int kQwzBlock = 256;
 
 constexpr int kMaxSpans = ZERO3_MAX_RANKS;
 
@@ -62,7 +68,9 @@ struct Span {
     float* m;
     float* v;
     void* out;           // sparam (bf16) or shard grad (kReduce)
-    const void* in;      // shard grad (kAdam) or sparam (kGather) or master (kCast)
+    const void* in;      // shard grad (kAdam) or sparam (kGather, kQuant) or master (kCast)
+    int8_t* codes;       // qwZ codes of the shard (kFusedQ, kQuant out; kDequant in)
+    float* scales;       // qwZ block scales of the shard
     int32_t vec;         // 1 when full chunks may use 16-byte vector accesses
     int32_t pad_;
 };

@@ -136,10 +136,28 @@ __device__ __forceinline__ float reduce1(const StreamArgs& a, int64_t off) {
 }
 
 template <int MODE, int ND, int GT>
-__device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp, int64_t i0) {
+__device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp, int64_t i0,
+                                             float* hq) {
     float g[8];
-    if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kReduce)
+    if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ || MODE == kReduce)
         reduce8<ND>(a, sp.gofs + i0, g);
+    if constexpr (MODE == kQuant) {
+        unpack8(ldcs16(static_cast<const uint16_t*>(sp.in) + i0), hq);
+        return;
+    }
+    if constexpr (MODE == kDequant) {
+        const uint2 q = __ldcs(reinterpret_cast<const uint2*>(sp.codes + i0));
+        const float sc = sp.scales[i0 / kQwzBlock];
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t w = e < 4 ? q.x : q.y;
+            const int8_t c = static_cast<int8_t>((w >> (8 * (e & 3))) & 0xffu);
+            y[e] = __fmul_rn(static_cast<float>(c), sc);
+        }
+        stcs16(a.full + sp.fofs + i0, pack8(y));
+        return;
+    }
 
     if constexpr (MODE == kReduce) {
         if constexpr (GT == ZERO3_BF16) {
@@ -193,6 +211,7 @@ __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp
         stcs_f4(sp.v + i0 + 4, make_float4(v[4], v[5], v[6], v[7]));
     }
     const uint4 h = pack8(p);
+    if constexpr (MODE == kFusedQ) unpack8(h, hq);
     if constexpr (MODE == kFusedRep) {
         // all-gather into every rank's full parameter copy
         const int nd = ND > 0 ? ND : a.nd;
@@ -208,12 +227,23 @@ __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp
 }
 
 template <int MODE, int ND, int GT>
-__device__ __forceinline__ void scalar_chunk(const StreamArgs& a, const Span& sp, int64_t i0) {
+__device__ __forceinline__ void scalar_chunk(const StreamArgs& a, const Span& sp, int64_t i0,
+                                             float* hq) {
     for (int e = 0; e < 8; ++e) {
         const int64_t i = i0 + e;
+        if constexpr (MODE == kFusedQ || MODE == kQuant) hq[e] = 0.0f;
         if (i < sp.lo || i >= sp.hi) continue;
+        if constexpr (MODE == kQuant) {
+            hq[e] = bf16_f32(static_cast<const uint16_t*>(sp.in)[i]);
+            continue;
+        }
+        if constexpr (MODE == kDequant) {
+            const float y = __fmul_rn(static_cast<float>(sp.codes[i]), sp.scales[i / kQwzBlock]);
+            a.full[sp.fofs + i] = to_bf16(y);
+            continue;
+        }
         float g = 0.0f;
-        if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kReduce)
+        if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ || MODE == kReduce)
             g = reduce1<ND>(a, sp.gofs + i);
         if constexpr (MODE == kReduce) {
             if constexpr (GT == ZERO3_BF16)
@@ -244,6 +274,7 @@ __device__ __forceinline__ void scalar_chunk(const StreamArgs& a, const Span& sp
             sp.v[i] = v;
         }
         const uint16_t h = to_bf16(p);
+        if constexpr (MODE == kFusedQ) hq[e] = bf16_f32(h);
         if constexpr (MODE == kFusedRep) {
             const int nd = ND > 0 ? ND : a.nd;
             for (int q = 0; q < nd; ++q) a.reps[q][sp.fofs + i] = h;
@@ -251,6 +282,34 @@ __device__ __forceinline__ void scalar_chunk(const StreamArgs& a, const Span& sp
             static_cast<uint16_t*>(sp.out)[i] = h;
             if (sp.fofs >= 0) a.full[sp.fofs + i] = h;
         }
+    }
+}
+
+// qwZ epilogue: the warp's 32 chunks are one 256-element block of one shard
+// (the launch numbers chunks that way).  absmax by warp shuffle, then
+// scale = absmax/127, code = round-half-even(x * 127/absmax), one binary32
+// operation each.  Every lane of the warp reaches the shuffles.
+__device__ __forceinline__ void qwz_block(const Span& sp, int64_t i0, const float* hq) {
+    float am = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(hq[e]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    const float inv = am > 0.0f ? __fdiv_rn(127.0f, am) : 0.0f;
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        int q = __float2int_rn(__fmul_rn(hq[e], inv));
+        q = q > 127 ? 127 : (q < -127 ? -127 : q);
+        w[e >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << (8 * (e & 3));
+    }
+    if (i0 >= sp.hi) return;  // chunk past the shard's end: nothing to store
+    if ((threadIdx.x & 31) == 0) sp.scales[i0 / kQwzBlock] = __fdiv_rn(am, 127.0f);
+    if (i0 + 8 <= sp.hi) {
+        *reinterpret_cast<uint2*>(sp.codes + i0) = make_uint2(w[0], w[1]);
+    } else {
+        for (int e = 0; e < 8 && i0 + e < sp.hi; ++e)
+            sp.codes[i0 + e] = static_cast<int8_t>((w[e >> 2] >> (8 * (e & 3))) & 0xffu);
     }
 }
 
@@ -263,10 +322,12 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const __grid_constant_
         while (s + 1 < a.n_spans && c >= a.span[s + 1].chunk0) ++s;
         const Span& sp = a.span[s];
         const int64_t i0 = (sp.lo & ~static_cast<int64_t>(7)) + ((c - sp.chunk0) << 3);
+        float hq[8];
         if (sp.vec && i0 >= sp.lo && i0 + 8 <= sp.hi)
-            vector_chunk<MODE, ND, GT>(a, sp, i0);
+            vector_chunk<MODE, ND, GT>(a, sp, i0, hq);
         else
-            scalar_chunk<MODE, ND, GT>(a, sp, i0);
+            scalar_chunk<MODE, ND, GT>(a, sp, i0, hq);
+        if constexpr (MODE == kFusedQ || MODE == kQuant) qwz_block(sp, i0, hq);
     }
 }
 
@@ -327,6 +388,9 @@ cudaError_t launch_stream(int mode, const StreamArgs& a, cudaStream_t stream) {
     switch (mode) {
         case kFused: return launch_nd<kFused, 0>(a, stream);
         case kFusedRep: return launch_nd<kFusedRep, 0>(a, stream);
+        case kFusedQ: return launch_nd<kFusedQ, 0>(a, stream);
+        case kQuant: return launch_one<kQuant, 1, 0>(a, stream);
+        case kDequant: return launch_one<kDequant, 1, 0>(a, stream);
         case kReduce:
             return a.dtype == ZERO3_BF16 ? launch_nd<kReduce, ZERO3_BF16>(a, stream)
                                          : launch_nd<kReduce, ZERO3_F32>(a, stream);

@@ -313,59 +313,83 @@ __device__ __forceinline__ void qwz_block(const Span& sp, int64_t i0, const floa
     }
 }
 
+// Chunks per thread.  The copy-like modes move few bytes per chunk (2-3 B
+// per element); a thread then takes 4 chunks, block-interleaved so every
+// warp instruction stays contiguous: measured +9% (gather) and +22%
+// (dequantizing all-gather) at 1.3B.  The fused modes keep one chunk per
+// thread (more registers per chunk; 2 per thread measured slightly slower).
+constexpr int kCopyChunks = 4;
+
+template <int MODE>
+__host__ __device__ constexpr int chunks_per_thread() {
+    return (MODE == kDequant || MODE == kGather) ? kCopyChunks : 1;
+}
+
 template <int MODE, int ND, int GT>
 __global__ void __launch_bounds__(kThreads) stream_kernel(const __grid_constant__ StreamArgs a) {
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    constexpr int CPT = chunks_per_thread<MODE>();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * CPT;
     int s = 0;
-    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-         c < a.total_chunks; c += stride) {
-        while (s + 1 < a.n_spans && c >= a.span[s + 1].chunk0) ++s;
-        const Span& sp = a.span[s];
-        const int64_t i0 = (sp.lo & ~static_cast<int64_t>(7)) + ((c - sp.chunk0) << 3);
-        float hq[8];
-        if (sp.vec && i0 >= sp.lo && i0 + 8 <= sp.hi)
-            vector_chunk<MODE, ND, GT>(a, sp, i0, hq);
-        else
-            scalar_chunk<MODE, ND, GT>(a, sp, i0, hq);
-        if constexpr (MODE == kFusedQ || MODE == kQuant) qwz_block(sp, i0, hq);
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * CPT + threadIdx.x;
+         base < a.total_chunks; base += stride) {
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            const int64_t c = base + static_cast<int64_t>(j) * blockDim.x;
+            if (c >= a.total_chunks) break;
+            while (s + 1 < a.n_spans && c >= a.span[s + 1].chunk0) ++s;
+            const Span& sp = a.span[s];
+            const int64_t i0 = (sp.lo & ~static_cast<int64_t>(7)) + ((c - sp.chunk0) << 3);
+            float hq[8];
+            if (sp.vec && i0 >= sp.lo && i0 + 8 <= sp.hi)
+                vector_chunk<MODE, ND, GT>(a, sp, i0, hq);
+            else
+                scalar_chunk<MODE, ND, GT>(a, sp, i0, hq);
+            if constexpr (MODE == kFusedQ || MODE == kQuant) qwz_block(sp, i0, hq);
+        }
     }
 }
 
 __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherArgs a) {
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * kCopyChunks;
     int s = 0;
-    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-         c < a.total_chunks; c += stride) {
-        while (s + 1 < a.n_segs && c >= a.seg[s + 1].chunk0) ++s;
-        const GatherSeg& g = a.seg[s];
-        const int64_t d0 = (g.dst_off & ~static_cast<int64_t>(7)) + ((c - g.chunk0) << 3);
-        const int64_t end = g.dst_off + g.len;
-        if (g.vec && d0 >= g.dst_off && d0 + 8 <= end) {
-            const uint4 x = ldcs16(g.src + (d0 - g.dst_off));
-            *reinterpret_cast<uint4*>(a.out + d0) = x;
-        } else {
-            for (int e = 0; e < 8; ++e) {
-                const int64_t d = d0 + e;
-                if (d >= g.dst_off && d < end) a.out[d] = g.src[d - g.dst_off];
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * kCopyChunks + threadIdx.x;
+         base < a.total_chunks; base += stride) {
+#pragma unroll
+        for (int j = 0; j < kCopyChunks; ++j) {
+            const int64_t c = base + static_cast<int64_t>(j) * blockDim.x;
+            if (c >= a.total_chunks) break;
+            while (s + 1 < a.n_segs && c >= a.seg[s + 1].chunk0) ++s;
+            const GatherSeg& g = a.seg[s];
+            const int64_t d0 = (g.dst_off & ~static_cast<int64_t>(7)) + ((c - g.chunk0) << 3);
+            const int64_t end = g.dst_off + g.len;
+            if (g.vec && d0 >= g.dst_off && d0 + 8 <= end) {
+                const uint4 x = ldcs16(g.src + (d0 - g.dst_off));
+                *reinterpret_cast<uint4*>(a.out + d0) = x;
+            } else {
+                for (int e = 0; e < 8; ++e) {
+                    const int64_t d = d0 + e;
+                    if (d >= g.dst_off && d < end) a.out[d] = g.src[d - g.dst_off];
+                }
             }
         }
     }
 }
 
-// One 8-element chunk per thread: the grid covers every chunk once (the
-// grid-stride loop in the kernels only matters beyond 2^31-1 blocks).
+// The grid covers every chunk once (the grid-stride loop in the kernels only
+// matters beyond 2^31-1 blocks).
 // Measured on GB300 at 1.3B / N_d = 8 this keeps more independent requests
 // in flight than an SM-sized persistent grid, whose threads serialise
 // load -> compute -> store per iteration: 7.2 TB/s against 6.5 TB/s.
-int grid_for(int64_t total_chunks) {
-    const int64_t need = (total_chunks + kThreads - 1) / kThreads;
+int grid_for(int64_t total_chunks, int chunks_per_thread = 1) {
+    const int64_t per = static_cast<int64_t>(kThreads) * chunks_per_thread;
+    const int64_t need = (total_chunks + per - 1) / per;
     const int64_t cap = 0x7fffffff;
     return static_cast<int>(need < cap ? need : cap);
 }
 
 template <int MODE, int ND, int GT>
 cudaError_t launch_one(const StreamArgs& a, cudaStream_t stream) {
-    const int grid = grid_for(a.total_chunks);
+    const int grid = grid_for(a.total_chunks, chunks_per_thread<MODE>());
     if (grid > 0) stream_kernel<MODE, ND, GT><<<grid, kThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
@@ -405,7 +429,7 @@ cudaError_t launch_stream(int mode, const StreamArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream) {
     if (a.total_chunks <= 0) return cudaSuccess;
-    const int grid = grid_for(a.total_chunks);
+    const int grid = grid_for(a.total_chunks, kCopyChunks);
     gather_kernel<<<grid, kThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }

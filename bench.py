@@ -37,6 +37,9 @@ WORKLOADS = {
                      "full emulation in one HBM"),
     "gpt2_small": ("gpt2_small", None, False,
                    "GPT-2-small list (12L, d=768, vocab 50257), N_d=4 virtual ranks"),
+    "llama_7b_full": ("llama_7b_full", None, True,
+                      "Llama-7B list, all N_d=8 ranks emulated in one HBM (~216 GB), "
+                      "one fused launch per 5e8-element bucket"),
     "llama_7b_rank0": ("llama_7b_rank0", [0], True,
                        "Llama-7B list (32L, d=4096, SwiGLU 11008, vocab 32000), rank-0 view at "
                        "N_d=8: rank 0's state resident, gradients per 5e8-element bucket"),
@@ -156,7 +159,8 @@ class ClockSampler:
 def make_workload(args):
     from zero_sharded_optimizer_shard_gb300 import workloads as W
     fac = WORKLOADS[args.workload][0]
-    w = W.llama_7b() if fac == "llama_7b_rank0" else getattr(W, fac)()
+    w = W.llama_7b(rank0_view=(fac == "llama_7b_rank0")) if fac.startswith("llama_7b") \
+        else getattr(W, fac)()
     if args.n_ranks:
         w.n_ranks = args.n_ranks
     if args.stage == 2:
@@ -628,7 +632,8 @@ def run_ours(args):
                            / (fused_launch_ms / 1e3)},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": profile_traffic(kernels_sha()),
+                         "traffic": profile_traffic(kernels_sha())
+                         if (args.workload == "decoder_1p3b" and not args.n_ranks) else None,
                          "kernel": "stream_kernel<kFused, N_d> (zero3_step)"},
             "gpu_launches": launches_per_step(e) * args.steps,
             "clocks": clk,
@@ -652,6 +657,11 @@ def run_e2e(e, w, args, stream, n_params, t0):
     import torch
     from zero_sharded_optimizer_shard_gb300 import zero3
     steps = max(2, min(args.steps, 6))
+    need = sum(x.numel() * 2 for G in e.grads for x in G) + e.full.numel() * 2
+    free, _ = torch.cuda.mem_get_info()
+    if need > free - (2 << 30):
+        return {"value": None, "unit": "params/s",
+                "note": f"second device buffer set ({need / 1e9:.0f} GB) does not fit"}
     try:
         host_g = [[torch.empty(x.numel(), dtype=x.dtype, pin_memory=True) for x in G] for G in e.grads]
         host_pg = [torch.empty(x.numel(), dtype=x.dtype, pin_memory=True) for x in e.pgrads]
@@ -671,6 +681,8 @@ def run_e2e(e, w, args, stream, n_params, t0):
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
     uploaded = [ev() for _ in range(steps)]
+    up_t = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(steps)]
     computed = [ev() for _ in range(steps)]
     read = [ev() for _ in range(steps)]
     torch.cuda.synchronize()
@@ -683,11 +695,13 @@ def run_e2e(e, w, args, stream, n_params, t0):
         with torch.cuda.stream(up):
             if k >= 2:
                 up.wait_event(computed[k - 2])  # buffer set b was read by step k-2
+            up_t[k][0].record(up)
             for hG, G in zip(host_g, dev_g[b]):
                 for h, d in zip(hG, G):
                     d.copy_(h, non_blocking=True)
             for h, d in zip(host_pg, dev_pg[b]):
                 d.copy_(h, non_blocking=True)
+            up_t[k][1].record(up)
             uploaded[k].record(up)
         stream.wait_event(uploaded[k])
         if k >= 2:
@@ -710,9 +724,12 @@ def run_e2e(e, w, args, stream, n_params, t0):
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     ms = start.elapsed_time(end) / steps
+    up_ms = [a.elapsed_time(b_) for a, b_ in up_t]
     return {"value": n_params / (ms / 1e3), "unit": "params/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms,
             "wall_ms_per_step": wall * 1e3 / steps,
+            "upload_ms_per_step": statistics.mean(up_ms),
+            "h2d_gbs": h2d / (statistics.mean(up_ms) / 1e3) / 1e9,
             "pipeline": "uploads of step k+1 and read-back of step k overlap step k"}
 
 

@@ -198,3 +198,18 @@ def test_ragged_2000_full():
         need = np.unique(np.concatenate(need))
         ps_param[need] = sampled_persistent_oracle(w, plan, need, T)[3]
     check_fetch(e, plan, w, T, None, ks, O.PersistState(None, None, None, ps_param))
+
+
+def test_llama_7b_full_emulation_max_size():
+    """Maximum size: all 8 ranks of the Llama-7B list in one HBM (about 216
+    GB: 108 GB of gradients, 81 GB of states, two 13.5 GB bf16 buffers),
+    bucketed launches; flat offsets and all-gather offsets run past 2^32
+    elements' bytes and 2^31 elements.  One step, sampled across every rank."""
+    w = W.llama_7b(rank0_view=False)
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    assert plan.psi_pad > 2 ** 32
+    e = run(w, 1, bucketed=True)
+    idx = sample_indices(plan, 0, plan.psi_pad, 60_000, 6)
+    assert idx.max() > 2 ** 32
+    check_sample(e, plan, w, idx, 1)
+    check_persistent(e, persistent_oracle(w, plan, 1))

@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--qwz", action="store_true",
                     help="ZeRO++ qwZ: the fused step emits int8 codes + block scales and the "
                          "all-gather dequantizes them into the full buffer")
+    ap.add_argument("--unfused", action="store_true",
+                    help="ablation: reduce-scatter (fp32 shard gradient), AdamW and all-gather "
+                         "as three launches, each timed")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -507,6 +510,69 @@ def run_qwz(args):
     return 0
 
 
+def run_unfused(args):
+    """Ablation: the same step as three launches (what fusion saves)."""
+    import torch
+    from zero_sharded_optimizer_shard_gb300 import build as b
+    b.build_all(quiet=True)
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+    torch.cuda.set_device(0)
+    w = make_workload(args)
+    stream = torch.cuda.Stream()
+    e = Emulation(w, stream=stream)
+    with torch.cuda.stream(stream):
+        e.init_params()
+        e.fill_grads(1)
+        sg = [torch.empty(e.S, dtype=torch.float32, device="cuda") for _ in range(e.nd)]
+    torch.cuda.synchronize()
+    lo, hi = e.chunks[0]
+    sgp = e.ptrs(sg)
+    ev = []
+
+    def step(t, timed):
+        x = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        x[0].record(stream)
+        zero3.zero3_reduce_scatter(e.plan, e.ptrs(e.grads[0]), lo, lo, hi, sgp, zero3.F32, e.sid)
+        x[1].record(stream)
+        zero3.zero3_adamw_step(e.plan, e.hp, t, sgp, zero3.F32, e.ptrs(e.master), e.ptrs(e.m),
+                               e.ptrs(e.v), e.ptrs(e.sparam), lo, hi, e.sid)
+        x[2].record(stream)
+        zero3.zero3_allgather(e.plan, e.ptrs(e.sparam), e.full.data_ptr(), lo, hi, e.sid)
+        x[3].record(stream)
+        zero3.zero3_step(e.plan, e.hp, t, e.ptrs(e.grads[0]), lo, e.ptrs(e.master), e.ptrs(e.m),
+                         e.ptrs(e.v), e.ptrs(e.sparam), e.full.data_ptr(), None, lo, hi, e.sid)
+        x[4].record(stream)
+        if timed:
+            ev.append(x)
+
+    t = 0
+    for _ in range(args.warmup):
+        t += 2
+        step(t, False)
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        t += 2
+        step(t, True)
+    torch.cuda.synchronize()
+    n = hi - lo
+    nd = w.n_ranks
+    parts = {"reduce_scatter": (0, 1, 2 * nd + 4), "adamw": (1, 2, 4 + 24 + 2),
+             "allgather": (2, 3, 2 + 2), "fused": (3, 4, 2 * nd + 28)}
+    peak, _ = peaks()
+    out = {}
+    for k, (i, j, bpe) in parts.items():
+        ms = statistics.mean(x[i].elapsed_time(x[j]) for x in ev)
+        gbs = n * bpe / (ms / 1e3) / 1e9
+        out[k] = {"ms": ms, "bytes_per_elem": bpe, "gbs": gbs, "frac": gbs / peak}
+    unf = sum(out[k]["ms"] for k in ("reduce_scatter", "adamw", "allgather"))
+    print(json.dumps({"metric": "unfused vs fused ZeRO-3 step (ablation)", "unit": "ms",
+                      "config": {"workload": WORKLOADS[args.workload][3], "elements": n},
+                      "kernels": out, "unfused_ms": unf, "fused_ms": out["fused"]["ms"],
+                      "fusion_speedup": unf / out["fused"]["ms"]}))
+    return 0
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -743,6 +809,8 @@ def main():
         return run_coordinator(args)
     if args.qwz:
         return run_qwz(args)
+    if args.unfused:
+        return run_unfused(args)
     return run_ours(args)
 
 

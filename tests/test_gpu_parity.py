@@ -87,11 +87,16 @@ def test_fused_step_matches_oracle(dev, wname, T):
     compare_all(e, plan, st, full, ps)
 
 
-@pytest.mark.parametrize("nd", [1, 2, 3, 5, 6, 8, 9, 16])
+@pytest.mark.parametrize("nd", [1, 2, 3, 5, 6, 8, 9, 16, 33, 64])
 def test_fused_step_rank_counts(dev, nd):
     """Specialised (1, 2, 4, 8) and generic rank counts; S not a multiple of 8
-    for most of them, so both the vector and the element paths run."""
-    w = W.mini_gpt(nd)
+    for most of them, so both the vector and the element paths run; 33 and 64
+    run the generic path with a partial last group of ranks and the maximum."""
+    if nd <= 16:
+        w = W.mini_gpt(nd)
+    else:
+        w = W.Workload(f"small_nd{nd}", [150_001, 123_457, 99_999, 7, 180_000], [0, 0, 1, 1, 2],
+                       n_ranks=nd, steps=3, seed=13)
     w.steps = 3
     plan, st, full, ps = oracle_run(w, 3)
     e = run_device(w, 3)
@@ -349,3 +354,44 @@ def test_stage12_step_matches_oracle(dev, nd):
         assert np.array_equal(bits(f32(e.master[q])), bits(st.master[q]))
         assert np.array_equal(bits(f32(e.m[q])), bits(st.m[q]))
         assert np.array_equal(bits(f32(e.v[q])), bits(st.v[q]))
+
+
+# ---------------------------------------------------------------- degenerate plans
+def test_all_persistent_plan(dev):
+    """Every tensor below the threshold: no flat range at all (psi_pad = 0),
+    zero3_step over the empty range still updates the persistent group."""
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    w = W.toy_mlp()
+    w.threshold = 10 ** 7
+    plan, st, full, ps = oracle_run(w, 3)
+    assert plan.psi_pad == 0 and plan.psi_s == w.psi
+    e = make_emu(w)
+    for t in range(1, 4):
+        e.fill_grads(t)
+        zero3.zero3_step(e.plan, e.hp, t, e.ptrs(e.pgrads), 0, [0] * 2, [0] * 2, [0] * 2,
+                         [0] * 2, 0, e.persist, 0, 0, e.sid)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(f32(e.pmaster)), bits(ps.master))
+    assert np.array_equal(u16(e.pparam), ps.param)
+    e.fetch(0)
+    torch.cuda.synchronize()
+    assert np.array_equal(u16(e.out)[:plan.submodule_numel(0)],
+                          O.fetch_submodule(plan, 0, st.sparam, ps.param))
+    e.release(0)
+
+
+def test_zero_size_tensors(dev):
+    """Zero-element tensors anywhere in the list (persistent by the strict
+    threshold) and a submodule made only of them: planner, step and fetch."""
+    numels = [0, 300_000, 0, 5, 0, 200_001, 0]
+    subs = [0, 0, 1, 1, 2, 3, 3]
+    w = W.Workload("zeros", numels, subs, n_ranks=3, steps=3, seed=11)
+    plan, st, full, ps = oracle_run(w, 3)
+    e = run_device(w, 3)
+    compare_all(e, plan, st, full, ps)
+    for k in range(plan.n_submodules):
+        e.fetch(k)
+        torch.cuda.synchronize()
+        n = plan.submodule_numel(k)
+        assert np.array_equal(u16(e.out)[:n], O.fetch_submodule(plan, k, st.sparam, ps.param))
+        e.release(k)

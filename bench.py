@@ -356,7 +356,7 @@ def run_coordinator(args):
     n_sub = plan.info.n_submodules
     sizes = [plan.submodule(k)[1] for k in range(n_sub)]
     trace = list(range(n_sub)) + list(reversed(range(n_sub)))
-    arena_elems = 3 * max(sizes)
+    arena_elems = (3 * max(sizes) + 7) // 8 * 8
     arena = torch.empty(arena_elems, dtype=torch.bfloat16, device="cuda")
     width = 1024
     X = torch.randn(args.tokens, width, dtype=torch.bfloat16, device="cuda")

@@ -330,7 +330,9 @@ zero3_status zero3_submodule_wait(zero3_plan* plan, int32_t k);
  * [hotelren], tuning list: stage3_prefetch_bucket_size,
  * stage3_max_live_parameters, stage3_max_reuse_distance).
  *  - Gathers run on prefetch_stream into a caller-owned arena (bf16,
- *    arena_elems >= the largest submodule); the compute stream waits on a
+ *    16-byte aligned, arena_elems >= the largest submodule rounded up to a
+ *    multiple of 8); each gathered copy occupies a whole number of 8-element
+ *    units so that it starts 16-byte aligned.  The compute stream waits on a
  *    submodule's ready event before its first use, so a fetch never blocks
  *    the host.  Ranges of the arena are reused only after the compute stream
  *    has passed the release of their previous contents.

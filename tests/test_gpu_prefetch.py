@@ -31,7 +31,7 @@ def run(w, steps, order_of_step, arena_mult=3.0, bucket=10**9, reuse=10**9, trac
     plan = e.plan
     n_sub = plan.info.n_submodules
     sizes = [plan.submodule(k)[1] for k in range(n_sub)]
-    arena_elems = int(max(sizes) * arena_mult)
+    arena_elems = (int(max(sizes) * arena_mult) + 7) // 8 * 8
     arena = torch.empty(arena_elems, dtype=torch.bfloat16, device="cuda")
     tr = fwd_bwd(n_sub) if trace == "given" else []
     co = zero3.Coordinator(plan, tr, e.ptrs(e.sparam), e.pparam.data_ptr(), arena.data_ptr(),
@@ -133,6 +133,7 @@ def test_state_errors():
     e = Emulation(w, stream=compute)
     e.init_params()
     n = max(e.plan.submodule(k)[1] for k in range(e.plan.info.n_submodules))
+    n = (n + 7) // 8 * 8
     arena = torch.empty(n, dtype=torch.bfloat16, device="cuda")
     co = zero3.Coordinator(e.plan, [0, 1, 2], e.ptrs(e.sparam), e.pparam.data_ptr(),
                            arena.data_ptr(), n, compute_stream=compute.cuda_stream,
@@ -146,7 +147,17 @@ def test_state_errors():
     assert exc.value.status == zero3.ESTATE
     # the arena holds one submodule: another fetch while 0 is held has no room
     with pytest.raises(zero3.Zero3Error) as exc:
-        co.fetch(0 if n == e.plan.submodule(1)[1] else 1)
-        co.fetch(2)
+        co.fetch(1)
     assert exc.value.status == zero3.ENOMEM
     torch.cuda.synchronize()
+
+
+def test_odd_sized_submodules_share_the_arena():
+    """Ragged submodule sizes with room for several copies at once: every
+    copy must start 16-byte aligned inside the arena (ranges are rounded to
+    8 elements) and hold the oracle's contents."""
+    w = W.ragged_small(7)
+    e, co, seen = run(w, 2, lambda t, n: fwd_bwd(n), arena_mult=4.0, delay=False)
+    plan, before = oracle_params_by_step(w, 2)
+    check(seen, plan, before)
+    assert co.stats()["prefetch_hits"] > 0

@@ -192,6 +192,9 @@ zero3_status check_gather_sources(const zero3_plan* p, int32_t k, const uint16_t
 
 zero3_status gather_submodule(const zero3_plan* p, int32_t k, const uint16_t* const* sparam,
                               const uint16_t* persist_param, uint16_t* out, cudaStream_t stream) {
+    // the kernel's chunks are 8-element units relative to `out`, stored 16
+    // bytes at a time: `out` must be 16-byte aligned
+    if (p->sub_numel[k] > 0 && (!out || !aligned16(out))) return ZERO3_EINVAL;
     GatherArgs a;
     std::memset(&a, 0, sizeof(a));
     a.out = out;

@@ -86,6 +86,11 @@ namespace {
 
 int64_t numel_of(const zero3_coordinator* c, int32_t k) { return c->plan->sub_numel[k]; }
 
+// Arena ranges are whole multiples of 8 elements (16 bytes), so every
+// gathered copy starts 16-byte aligned like the arena itself: the gather
+// kernel's vector path stores 16 bytes at a time relative to that start.
+int64_t span_of(const zero3_coordinator* c, int32_t k) { return (numel_of(c, k) + 7) / 8 * 8; }
+
 void free_insert(zero3_coordinator* c, int64_t off, int64_t len, uint64_t seq) {
     if (len <= 0) return;
     auto& fl = c->free_list;
@@ -134,7 +139,7 @@ zero3_status drop(zero3_coordinator* c, int32_t k) {
     uint64_t seq = 0;
     zero3_status st = record_release(c, &seq);
     if (st != ZERO3_OK) return st;
-    free_insert(c, c->off[k], numel_of(c, k), seq);
+    free_insert(c, c->off[k], span_of(c, k), seq);
     c->live -= numel_of(c, k);
     if (c->ahead[k]) c->ahead_elems -= numel_of(c, k);
     c->ahead[k] = 0;
@@ -173,7 +178,7 @@ zero3_status gather(zero3_coordinator* c, int32_t k, bool evict) {
     for (;;) {
         uint64_t seq = 0;
         const bool budget = c->live + n <= c->cfg.max_live_parameters;
-        const int64_t o = budget ? free_take(c, n, &seq) : -1;
+        const int64_t o = budget ? free_take(c, span_of(c, k), &seq) : -1;
         if (o >= 0) {
             if (seq > 0 &&
                 cudaStreamWaitEvent(c->prefetch, c->rel[seq % kReleaseRing], 0) != cudaSuccess)
@@ -254,6 +259,7 @@ zero3_status zero3_coordinator_create(zero3_plan* plan, const int32_t* trace, in
     const int32_t n_sub = static_cast<int32_t>(plan->sub_tensors.size());
     int64_t biggest = 0;
     for (int32_t k = 0; k < n_sub; ++k) biggest = std::max(biggest, plan->sub_numel[k]);
+    const int64_t biggest_span = (biggest + 7) / 8 * 8;
     // the sources of every submodule, checked once
     for (int64_t t = 0; t < static_cast<int64_t>(plan->numel.size()); ++t) {
         if (plan->numel[t] == 0) continue;
@@ -268,7 +274,7 @@ zero3_status zero3_coordinator_create(zero3_plan* plan, const int32_t* trace, in
             }
         }
     }
-    if (biggest > arena_elems || biggest > cfg->max_live_parameters) return ZERO3_EINVAL;
+    if (biggest_span > arena_elems || biggest > cfg->max_live_parameters) return ZERO3_EINVAL;
     for (int64_t j = 0; j < n_trace; ++j)
         if (trace[j] < 0 || trace[j] >= n_sub) return ZERO3_EINVAL;
 
@@ -293,7 +299,8 @@ zero3_status zero3_coordinator_create(zero3_plan* plan, const int32_t* trace, in
         c->off.assign(n_sub, -1);
         c->ahead.assign(n_sub, 0);
         c->ready.assign(n_sub, nullptr);
-        if (arena_elems > 0) c->free_list.push_back(FreeRange{0, arena_elems, 0});
+        // only whole 8-element units of the arena are handed out
+        if (arena_elems >= 8) c->free_list.push_back(FreeRange{0, arena_elems / 8 * 8, 0});
     } catch (const std::bad_alloc&) {
         delete c;
         return ZERO3_ENOMEM;

@@ -29,12 +29,22 @@ def _ptr(t: Optional[torch.Tensor]) -> int:
     return t.data_ptr() if t is not None else 0
 
 
+# Sentinels of the guard bands (bit patterns; NaN payloads for the floats).
+_SENTINEL = {torch.float32: 0x7FC0DEAD, torch.bfloat16: 0x7FAD, torch.int8: 0x5A}
+_INT_VIEW = {torch.float32: torch.int32, torch.bfloat16: torch.int16, torch.int8: torch.int8}
+
+
 class Emulation:
     def __init__(self, w: Workload, device: str = "cuda", state_ranks: Optional[Sequence[int]] = None,
                  bucketed: bool = False, stream: Optional[torch.cuda.Stream] = None,
-                 alloc_grads: bool = True):
+                 alloc_grads: bool = True, guard: int = 0):
+        """guard > 0 surrounds every buffer with `guard` sentinel elements on
+        each side (guard-band canaries); check_guards() reports any band a
+        call has written into."""
         self.w = w
         self.dev = torch.device(device)
+        self.guard = guard
+        self._guarded = []
         self.plan = zero3.Plan(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
         info = self.plan.info
         self.nd = w.n_ranks
@@ -53,32 +63,56 @@ class Emulation:
             self.chunks = list(zip(cuts[:-1], cuts[1:]))
         else:
             self.chunks = [(lo, hi)] if hi > lo else []
-        e = dict(device=self.dev)
         bf, f32 = torch.bfloat16, torch.float32
+        A = self.alloc
         self.grads: List[List[torch.Tensor]] = []
         if alloc_grads:
             for (a, b) in self.chunks:
-                self.grads.append([torch.empty(b - a, dtype=bf, **e) for _ in range(self.nd)])
-        self.pgrads = [torch.empty(self.psi_s, dtype=bf, **e) for _ in range(self.nd)]
+                self.grads.append([A(b - a, bf) for _ in range(self.nd)])
+        self.pgrads = [A(self.psi_s, bf) for _ in range(self.nd)]
         self.master: List[Optional[torch.Tensor]] = [None] * self.nd
         self.m: List[Optional[torch.Tensor]] = [None] * self.nd
         self.v: List[Optional[torch.Tensor]] = [None] * self.nd
         for r in self.state_ranks:
-            self.master[r] = torch.empty(self.S, dtype=f32, **e)
-            self.m[r] = torch.zeros(self.S, dtype=f32, **e)
-            self.v[r] = torch.zeros(self.S, dtype=f32, **e)
-        self.sparam = [torch.empty(self.S, dtype=bf, **e) for _ in range(self.nd)]
-        self.full = torch.zeros(self.psi_pad, dtype=bf, **e)
-        self.pmaster = torch.empty(self.psi_s, dtype=f32, **e)
-        self.pm = torch.zeros(self.psi_s, dtype=f32, **e)
-        self.pv = torch.zeros(self.psi_s, dtype=f32, **e)
-        self.pparam = torch.empty(self.psi_s, dtype=bf, **e)
+            self.master[r] = A(self.S, f32)
+            self.m[r] = A(self.S, f32, zero=True)
+            self.v[r] = A(self.S, f32, zero=True)
+        self.sparam = [A(self.S, bf) for _ in range(self.nd)]
+        self.full = A(self.psi_pad, bf, zero=True)
+        self.pmaster = A(self.psi_s, f32)
+        self.pm = A(self.psi_s, f32, zero=True)
+        self.pv = A(self.psi_s, f32, zero=True)
+        self.pparam = A(self.psi_s, bf)
         self.max_sub = max([self.plan.submodule(k)[1] for k in range(info.n_submodules)] + [0])
-        self.out = torch.empty(max(self.max_sub, 1), dtype=bf, **e)
+        self.out = A(max(self.max_sub, 1), bf)
         self.persist = zero3.persist_state([_ptr(g) for g in self.pgrads], _ptr(self.pmaster),
                                            _ptr(self.pm), _ptr(self.pv), _ptr(self.pparam))
 
     # ------------------------------------------------------------ plumbing
+    def alloc(self, n: int, dtype, zero: bool = False) -> torch.Tensor:
+        """A device buffer of n elements (16-byte aligned); with guard bands
+        when the emulation was created with guard > 0."""
+        g = self.guard
+        if g <= 0:
+            return (torch.zeros if zero else torch.empty)(n, dtype=dtype, device=self.dev)
+        base = torch.empty(n + 2 * g, dtype=dtype, device=self.dev)
+        base.view(_INT_VIEW[dtype]).fill_(_SENTINEL[dtype])
+        view = base[g:g + n]
+        if zero:
+            view.zero_()
+        self._guarded.append((base, g, n, dtype))
+        return view
+
+    def check_guards(self) -> List[str]:
+        """Names of the buffers whose guard bands were written."""
+        bad = []
+        for i, (base, g, n, dtype) in enumerate(self._guarded):
+            iv = base.view(_INT_VIEW[dtype])
+            want = _SENTINEL[dtype]
+            if not (bool((iv[:g] == want).all()) and bool((iv[g + n:] == want).all())):
+                bad.append(f"buffer {i} ({dtype}, {n} elements)")
+        return bad
+
     @property
     def sid(self) -> int:
         s = self.stream if self.stream is not None else torch.cuda.current_stream(self.dev)

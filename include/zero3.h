@@ -414,10 +414,15 @@ void zero3_coordinator_destroy(zero3_coordinator* c);
  * save_checkpoint / load_checkpoint write and read every partition), or the
  * weights are gathered into complete 16-bit tensors on save ([hotelren],
  * stage3_gather_16bit_weights_on_model_save; [baike] section 应用).
- * A file is a 48-byte header (magic "ZERO3CKP", version 1, kind, rank,
- * n_ranks, element count, step t, fingerprint of the partition: rank count,
- * threshold and every tensor's element count) followed by raw little-endian
- * arrays.  Loading checks every header field against the plan and the
+ * A file is a 48-byte little-endian header
+ *   char magic[8] = "ZERO3CKP"; uint32 version = 1; uint32 kind (1 shard,
+ *   2 persistent group, 3 16-bit weights, 4 fp32 weights); int32 rank (-1 when
+ *   not a shard); int32 n_ranks; int64 element count; int64 step t;
+ *   uint64 fingerprint = FNV-1a 64 (offset basis 14695981039346656037,
+ *   prime 1099511628211) over the bytes of the int64 values n_ranks,
+ *   persistence threshold, tensor count, then every tensor's element count
+ * followed by raw little-endian arrays (a shard: fp32 master, m, v of S
+ * elements each; the persistent group likewise with psi_s elements).  Loading checks every header field against the plan and the
  * arguments and returns ZERO3_EIO on any mismatch, on a short file or on
  * trailing bytes; nothing is written to device memory before the header has
  * been validated.  Calls are synchronous (they synchronise `stream`); device
@@ -452,6 +457,17 @@ zero3_status zero3_save_16bit_weights(const zero3_plan* plan, const uint16_t* fu
                                       const uint16_t* persist_param, const char* path,
                                       zero3_stream stream);
 
+/* Offline merge of partition-wise checkpoints into complete fp32 weights
+ * ([baike] section 应用: save the shard weights, then merge them with the
+ * accompanying script).  Host only, no GPU: reads the fp32 master array of
+ * the N_d shard files (shard_paths[r] written by zero3_save_shard for rank r)
+ * and of the persistent file (NULL allowed when psi_s = 0), and writes kind 4
+ * with every tensor complete, in list order, as fp32.  All inputs are
+ * validated (headers, ranks, partition, equal step counts) before the output
+ * is created; ZERO3_EIO otherwise.  Memory use is one 16 MiB buffer. */
+zero3_status zero3_merge_shards(const zero3_plan* plan, const char* const* shard_paths,
+                                const char* persistent_path, const char* out_path);
+
 /* ------------------------------------------------------------- accounting */
 
 /* Model-state bytes per rank, 2-byte params and grads plus 12 bytes of Adam
@@ -459,6 +475,11 @@ zero3_status zero3_save_16bit_weights(const zero3_plan* plan, const uint16_t* fu
  * [compass] section 三階段記憶體公式彙總): stage 0 16Ψ, stage 1 4Ψ+12Ψ/N_d,
  * stage 2 2Ψ+14Ψ/N_d, stage 3 16Ψ/N_d.  EINVAL for other stages or n_d < 1. */
 zero3_status zero3_memory_bytes(int32_t stage, double psi, int32_t n_d, double* bytes_per_rank);
+
+/* Model-state bytes one rank holds for this plan: zero3_memory_bytes on the
+ * padded partitioned elements (psi_pad) plus the persistent group, which every
+ * rank keeps whole at 2 + 2 + 12 bytes per element. */
+zero3_status zero3_plan_memory_bytes(const zero3_plan* plan, int32_t stage, double* bytes_per_rank);
 
 /* Elements sent per rank per step by ring collectives ([111qqz] section
  * "为什么 ZeRO-2 的通信量和 DDP 接近", V = (N-1)/N * S; [compass] section

@@ -20,6 +20,8 @@ What it computes, with the passages each part follows:
 * replicated_step -- the ZeRO-1/2 step: every rank keeps full parameters.
 * fetch_submodule -- gather a submodule's shards into one contiguous tensor.
 * gather_16bit_weights -- every tensor complete, in list order (save).
+* merge_fp32_weights -- offline merge of partition-wise fp32 shards.
+* plan_memory_bytes -- per-rank model-state bytes of a concrete plan.
 * qwz_quantize, qwz_dequantize, qwz_allgather -- the int8 quantized
                    parameter all-gather of ZeRO++ (qwZ).
 * memory_bytes, comm_elems, ring_send_bytes -- the model-state and
@@ -546,6 +548,40 @@ def gather_16bit_weights(plan: Plan, sparam: Sequence[np.ndarray],
                     w[sel] = np.asarray(sparam[r])[f[sel] - r * S]
             out.append(w)
     return out
+
+
+def merge_fp32_weights(plan: Plan, masters: Sequence[np.ndarray],
+                       persist_master: np.ndarray) -> List[np.ndarray]:
+    """Consolidate the per-rank fp32 master shards into complete fp32 tensors
+    in list order: the offline merge of partition-wise checkpoints into full
+    weights (encyclopedia entry, section 应用: save the shard weights, then
+    merge them with the accompanying script).  Same element mapping as
+    gather_16bit_weights, on the fp32 masters."""
+    S = plan.shard_len
+    out = []
+    for t in range(len(plan.numel)):
+        n = plan.numel[t]
+        if plan.persistent[t]:
+            o = plan.offset[t]
+            out.append(np.asarray(persist_master[o:o + n], np.float32).copy())
+        else:
+            f = np.arange(plan.offset[t], plan.offset[t] + n, dtype=np.int64)
+            w = np.empty(n, np.float32)
+            for r in range(plan.n_ranks):
+                sel = (f // S) == r
+                if sel.any():
+                    w[sel] = np.asarray(masters[r])[f[sel] - r * S]
+            out.append(w)
+    return out
+
+
+def plan_memory_bytes(plan: Plan, stage: int, K: int = 12) -> float:
+    """Model-state bytes one rank holds for this plan: the closed forms of
+    memory_bytes applied to the padded partitioned elements, plus the
+    persistent group, which every rank keeps whole (2 + 2 + K bytes per
+    element) at every stage ("DeepSpeed Zero-3 的参数分区与按需访问机制",
+    小参数驻留: small parameters stay resident on every card)."""
+    return memory_bytes(stage, plan.psi_pad, plan.n_ranks, K) + (2 + 2 + K) * plan.psi_s
 
 
 class SubmoduleStates:

@@ -295,3 +295,72 @@ def test_coordinator_create_rejects_bad_arguments(lib):
     assert create(sparam=None) == E
     assert create(arena=MISALIGNED) == E
     assert create(persist=0) == E                       # submodule 0 holds a persistent tensor
+
+
+# ---------------------------------------------------------------- offline merge and plan memory
+def _fnv1a(values):
+    h = 14695981039346656037
+    for x in values:
+        for b in int(x).to_bytes(8, "little", signed=True):
+            h ^= b
+            h = (h * 1099511628211) & 0xFFFFFFFFFFFFFFFF
+    return h
+
+
+def _write(path, kind, rank, nd, n, t, fp, arrays):
+    import struct
+    with open(path, "wb") as f:
+        f.write(struct.pack("<8sIIiiqqQ", b"ZERO3CKP", 1, kind, rank, nd, n, t, fp))
+        for a in arrays:
+            f.write(np.ascontiguousarray(a, np.float32).tobytes())
+
+
+def test_merge_shards_matches_oracle(lib, tmp_path):
+    """Shard files written from the documented format (host only) are
+    merged by the library into the oracle's consolidated fp32 weights."""
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    w = W.ragged_small(7)
+    ref = O.partition(w.numels, w.submodule_of, 7, w.threshold, w.bucket)
+    p = zero3.Plan(w.numels, w.submodule_of, 7, w.threshold, w.bucket)
+    fp = _fnv1a([7, w.threshold, len(w.numels)] + list(w.numels))
+    rng = np.random.default_rng(0)
+    masters = [rng.standard_normal(ref.shard_len).astype(np.float32) for _ in range(7)]
+    pm = rng.standard_normal(ref.psi_s).astype(np.float32)
+    paths = []
+    for r in range(7):
+        paths.append(tmp_path / f"r{r}.ckpt")
+        _write(paths[-1], 1, r, 7, ref.shard_len, 9, fp,
+               [masters[r], np.zeros(ref.shard_len), np.ones(ref.shard_len)])
+    _write(tmp_path / "p.ckpt", 2, -1, 7, ref.psi_s, 9, fp, [pm, np.zeros(ref.psi_s), np.zeros(ref.psi_s)])
+    out = tmp_path / "merged.bin"
+    zero3.zero3_merge_shards(p, paths, tmp_path / "p.ckpt", out)
+    raw = out.read_bytes()
+    import struct
+    magic, ver, kind, rank, nd, n, t, fph = struct.unpack_from("<8sIIiiqqQ", raw)
+    assert (magic, ver, kind, nd, n, t, fph) == (b"ZERO3CKP", 1, 4, 7, sum(w.numels), 9, fp)
+    got = np.frombuffer(raw, np.float32, offset=48)
+    want = np.concatenate(O.merge_fp32_weights(ref, masters, pm))
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    # a shard of another step, a missing rank file, or a wrong rank: EIO, no output
+    _write(paths[3], 1, 3, 7, ref.shard_len, 8, fp, [masters[3]] * 3)
+    out2 = tmp_path / "merged2.bin"
+    with pytest.raises(zero3.Zero3Error) as exc:
+        zero3.zero3_merge_shards(p, paths, tmp_path / "p.ckpt", out2)
+    assert exc.value.status == zero3.EIO and not out2.exists()
+    swapped = list(paths)
+    swapped[1], swapped[2] = swapped[2], swapped[1]
+    with pytest.raises(zero3.Zero3Error):
+        zero3.zero3_merge_shards(p, swapped, tmp_path / "p.ckpt", out2)
+    with pytest.raises(zero3.Zero3Error):
+        zero3.zero3_merge_shards(p, paths[:6] + [tmp_path / "nope"], tmp_path / "p.ckpt", out2)
+
+
+def test_plan_memory_bytes_matches_oracle(lib):
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    for name in ("toy_mlp", "gpt2_small", "decoder_1p3b", "llama_7b_rank0", "ragged"):
+        w = W.BY_NAME[name]()
+        ref = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+        p = zero3.Plan(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+        for stage in range(4):
+            assert zero3.zero3_plan_memory_bytes(p, stage) == pytest.approx(
+                O.plan_memory_bytes(ref, stage), rel=1e-15)

@@ -379,6 +379,13 @@ def test_partition_brute_force(nd):
         # consolidated 16-bit weights: every tensor complete, in list order
         whole = O.gather_16bit_weights(plan, sparam, pp)
         assert len(whole) == n_t and all(np.array_equal(a, b) for a, b in zip(whole, vals))
+        # the fp32 merge uses the same mapping on float shards
+        fvals = [v.astype(np.float32) * np.float32(0.5) for v in vals]
+        fsh = [np.array([0 if lab is None else fvals[lab[0]][lab[1]] for lab in shards[r]], np.float32)
+               for r in range(nd)]
+        fpp = np.concatenate([fvals[t] for t in range(n_t) if numels[t] < thr] + [np.zeros(0, np.float32)])
+        merged = O.merge_fp32_weights(plan, fsh, fpp)
+        assert all(np.array_equal(a, b) for a, b in zip(merged, fvals))
 
 
 def test_workload_sizes():
@@ -464,3 +471,17 @@ def test_qwz_allgather_layout():
     S = plan.shard_len
     for r in range(3):
         assert np.array_equal(full[r * S:(r + 1) * S], O.qwz_dequantize(*q[r]))
+
+
+def test_plan_memory_reduces_to_closed_form():
+    """No persistent tensors and no padding: the plan's per-rank bytes are
+    the closed forms; the 7B / 4-GPU plan gives the pages' 28 GB at stage 3.
+    Padding and persistent tensors add exactly their own bytes."""
+    plan = O.partition([7_000_000_000], None, 4, threshold=0)
+    assert O.plan_memory_bytes(plan, 3) == 28e9
+    assert O.plan_memory_bytes(plan, 2) == 38.5e9
+    assert O.plan_memory_bytes(plan, 1) == 49e9
+    assert O.plan_memory_bytes(plan, 0) == 112e9
+    plan = O.partition([1001, 50], None, 4, threshold=100)
+    assert plan.psi_pad == 1004 and plan.psi_s == 50
+    assert O.plan_memory_bytes(plan, 3) == 16 * 1004 / 4 + 16 * 50

@@ -22,7 +22,7 @@ namespace {
 
 constexpr char kMagic[8] = {'Z', 'E', 'R', 'O', '3', 'C', 'K', 'P'};
 constexpr uint32_t kVersion = 1;
-enum Kind : uint32_t { kShard = 1, kPersist = 2, kWeights16 = 3 };
+enum Kind : uint32_t { kShard = 1, kPersist = 2, kWeights16 = 3, kWeights32 = 4 };
 constexpr int64_t kStage = int64_t(16) << 20;  // bytes per host staging chunk
 
 struct Header {
@@ -39,7 +39,7 @@ static_assert(sizeof(Header) == 48, "checkpoint header layout");
 
 // FNV-1a over the values that fix the partition.
 uint64_t fingerprint(const zero3_plan* p) {
-    uint64_t h = 1469598103934665603ull;
+    uint64_t h = 14695981039346656037ull;  // FNV-1a 64 offset basis
     auto mix = [&h](int64_t x) {
         for (int k = 0; k < 8; ++k) {
             h ^= static_cast<uint64_t>((x >> (8 * k)) & 0xff);
@@ -68,6 +68,9 @@ Header make_header(const zero3_plan* p, Kind kind, int32_t rank, int64_t n, int6
 
 struct File {
     FILE* f = nullptr;
+    File() = default;
+    File(const File&) = delete;
+    File& operator=(const File&) = delete;
     ~File() {
         if (f) std::fclose(f);
     }
@@ -160,6 +163,19 @@ zero3_status load_arrays(const zero3_plan* p, const char* path, Kind kind, int32
     return ZERO3_OK;
 }
 
+// Copies `bytes` from file `in` at byte offset `off` to `out`.
+zero3_status copy_range(FILE* in, int64_t off, int64_t bytes, FILE* out, std::vector<char>& buf) {
+    if (std::fseek(in, static_cast<long>(off), SEEK_SET) != 0) return ZERO3_EIO;
+    while (bytes > 0) {
+        const int64_t n = bytes < static_cast<int64_t>(buf.size()) ? bytes
+                                                                   : static_cast<int64_t>(buf.size());
+        if (std::fread(buf.data(), 1, n, in) != static_cast<size_t>(n)) return ZERO3_EIO;
+        if (std::fwrite(buf.data(), 1, n, out) != static_cast<size_t>(n)) return ZERO3_EIO;
+        bytes -= n;
+    }
+    return ZERO3_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -225,6 +241,62 @@ zero3_status zero3_save_16bit_weights(const zero3_plan* p, const uint16_t* full,
         if (st != ZERO3_OK) return st;
     }
     if (std::fflush(file.f) != 0) return ZERO3_EIO;
+    return ZERO3_OK;
+}
+
+zero3_status zero3_merge_shards(const zero3_plan* p, const char* const* shard_paths,
+                               const char* persistent_path, const char* out_path) {
+    if (!p || !shard_paths || !out_path) return ZERO3_EINVAL;
+    if (p->psi_s > 0 && !persistent_path) return ZERO3_EINVAL;
+    for (int r = 0; r < p->n_ranks; ++r)
+        if (!shard_paths[r]) return ZERO3_EINVAL;
+    // open and validate every input before writing anything
+    std::vector<File> shards(p->n_ranks);
+    int64_t t = -1;
+    for (int r = 0; r < p->n_ranks; ++r) {
+        Header h;
+        zero3_status st = open_checked(p, shard_paths[r], kShard, r, p->S, shards[r], h);
+        if (st != ZERO3_OK) return st;
+        if (t >= 0 && h.t != t) return ZERO3_EIO;  // shards of different steps
+        t = h.t;
+    }
+    File pers;
+    if (p->psi_s > 0) {
+        Header h;
+        zero3_status st = open_checked(p, persistent_path, kPersist, -1, p->psi_s, pers, h);
+        if (st != ZERO3_OK) return st;
+        if (t >= 0 && h.t != t) return ZERO3_EIO;
+        t = h.t;
+    }
+    File out;
+    out.f = std::fopen(out_path, "wb");
+    if (!out.f) return ZERO3_EIO;
+    const Header h = make_header(p, kWeights32, -1, p->psi_p + p->psi_s, t < 0 ? 0 : t);
+    if (std::fwrite(&h, sizeof(h), 1, out.f) != 1) return ZERO3_EIO;
+    std::vector<char> buf;
+    try {
+        buf.resize(kStage);
+    } catch (const std::bad_alloc&) {
+        return ZERO3_ENOMEM;
+    }
+    // each tensor in list order; a shard file holds master, m, v: the master
+    // array starts right after the header
+    for (size_t ti = 0; ti < p->numel.size(); ++ti) {
+        zero3_status st = ZERO3_OK;
+        if (p->persistent[ti]) {
+            st = copy_range(pers.f, static_cast<int64_t>(sizeof(Header)) + p->offset[ti] * 4,
+                            p->numel[ti] * 4, out.f, buf);
+        } else {
+            for (int64_t sgi = p->seg_begin[ti]; sgi < p->seg_begin[ti + 1] && st == ZERO3_OK; ++sgi) {
+                const zero3_segment& sg = p->segs[sgi];
+                st = copy_range(shards[sg.rank].f,
+                                static_cast<int64_t>(sizeof(Header)) + sg.shard_off * 4,
+                                sg.len * 4, out.f, buf);
+            }
+        }
+        if (st != ZERO3_OK) return st;
+    }
+    if (std::fflush(out.f) != 0) return ZERO3_EIO;
     return ZERO3_OK;
 }
 

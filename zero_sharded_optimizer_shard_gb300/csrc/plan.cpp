@@ -220,6 +220,17 @@ zero3_status zero3_memory_bytes(int32_t stage, double psi, int32_t n_d, double* 
     return ZERO3_OK;
 }
 
+zero3_status zero3_plan_memory_bytes(const zero3_plan* p, int32_t stage, double* bytes) {
+    // closed form on the padded partitioned elements + the persistent group,
+    // which every rank keeps whole (2 + 2 + 12 bytes per element)
+    if (!p || !bytes) return ZERO3_EINVAL;
+    double part = 0.0;
+    zero3_status st = zero3_memory_bytes(stage, static_cast<double>(p->psi_pad), p->n_ranks, &part);
+    if (st != ZERO3_OK) return st;
+    *bytes = part + 16.0 * static_cast<double>(p->psi_s);
+    return ZERO3_OK;
+}
+
 zero3_status zero3_comm_elems(int32_t stage, double psi, int32_t n_d, double* elems) {
     // reduce-scatter + all-gather = 2Ψ; stage 3 gathers parameters twice.
     if (!elems || n_d < 1 || !(psi >= 0.0)) return ZERO3_EINVAL;

@@ -130,6 +130,8 @@ _SIGS = [
     ("zero3_save_persistent", C.c_int, [_vp, C.c_int64, C.POINTER(PersistState), C.c_char_p, _vp]),
     ("zero3_load_persistent", C.c_int, [_vp, _c_i64_p, C.POINTER(PersistState), C.c_char_p, _vp]),
     ("zero3_save_16bit_weights", C.c_int, [_vp, _vp, _vp, C.c_char_p, _vp]),
+    ("zero3_merge_shards", C.c_int, [_vp, C.POINTER(C.c_char_p), C.c_char_p, C.c_char_p]),
+    ("zero3_plan_memory_bytes", C.c_int, [_vp, C.c_int32, C.POINTER(C.c_double)]),
     ("zero3_memory_bytes", C.c_int, [C.c_int32, C.c_double, C.c_int32, C.POINTER(C.c_double)]),
     ("zero3_comm_elems", C.c_int, [C.c_int32, C.c_double, C.c_int32, C.POINTER(C.c_double)]),
     ("zero3_sync", C.c_int, [_vp]),
@@ -405,6 +407,20 @@ def zero3_load_persistent(plan: Plan, persist, path, stream=0) -> int:
 def zero3_save_16bit_weights(plan: Plan, full, persist_param, path, stream=0):
     _check(plan._lib.zero3_save_16bit_weights(plan.handle, full or None, persist_param or None,
                                               _path(path), stream), "zero3_save_16bit_weights")
+
+
+def zero3_merge_shards(plan: Plan, shard_paths, persistent_path, out_path):
+    arr = (C.c_char_p * len(shard_paths))(*[_path(x) for x in shard_paths])
+    _check(plan._lib.zero3_merge_shards(plan.handle, arr,
+                                        _path(persistent_path) if persistent_path else None,
+                                        _path(out_path)), "zero3_merge_shards")
+
+
+def zero3_plan_memory_bytes(plan: Plan, stage) -> float:
+    out = C.c_double()
+    _check(plan._lib.zero3_plan_memory_bytes(plan.handle, stage, C.byref(out)),
+           "zero3_plan_memory_bytes")
+    return out.value
 
 
 def zero3_memory_bytes(stage, psi, n_d) -> float:

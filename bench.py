@@ -268,24 +268,36 @@ def launches_per_step(e) -> int:
     return n + len(e.chunks) + (1 if e.psi_s > 0 else 0)
 
 
+def setup_single(args, stream=None, **emu_kw):
+    """Build the library, create the workload's emulation on cuda:0 and fill
+    its inputs (shared by the single-GPU measurement modes)."""
+    import torch
+    from zero_sharded_optimizer_shard_gb300 import build as b
+    b.build_all(quiet=True)
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+    torch.cuda.set_device(0)
+    fac, state_ranks, bucketed, desc = WORKLOADS[args.workload]
+    w = make_workload(args)
+    stream = stream or torch.cuda.Stream()
+    kw = dict(state_ranks=state_ranks, bucketed=bucketed)
+    kw.update(emu_kw)
+    e = Emulation(w, stream=stream, **kw)
+    with torch.cuda.stream(stream):
+        e.init_params()
+        e.fill_grads(1)
+    torch.cuda.synchronize()
+    return w, e, stream, desc
+
+
 def run_stage12(args):
     """The ZeRO-1/2 step: every rank keeps full bf16 parameters, so a step is
     the fused reduce-scatter + AdamW + all-gather into all N_d copies."""
     import torch
-    from zero_sharded_optimizer_shard_gb300 import build as b
-    b.build_all(quiet=True)
     from zero_sharded_optimizer_shard_gb300 import zero3
-    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
-    torch.cuda.set_device(0)
-    fac, state_ranks, bucketed, desc = WORKLOADS[args.workload]
-    if state_ranks is not None:
+    if WORKLOADS[args.workload][1] is not None:
         raise SystemExit("--stage 2 needs a full emulation workload")
-    w = make_workload(args)
-    stream = torch.cuda.Stream()
-    e = Emulation(w, stream=stream)
+    w, e, stream, desc = setup_single(args, bucketed=False)
     with torch.cuda.stream(stream):
-        e.init_params()
-        e.fill_grads(1)
         params = [e.full.clone() for _ in range(w.n_ranks)]
     e.sparam = e.full = None  # stage 1/2 keeps no separate shard or gathered buffer
     torch.cuda.synchronize()
@@ -341,17 +353,11 @@ def run_coordinator(args):
     prefetch off (every gather on demand), and the GEMMs alone (no gathers);
     the difference off - on is the gather time the prefetch hides."""
     import torch
-    from zero_sharded_optimizer_shard_gb300 import build as b
-    b.build_all(quiet=True)
     from zero_sharded_optimizer_shard_gb300 import zero3
-    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
-    torch.cuda.set_device(0)
-    w = make_workload(args)
-    compute, prefetch = torch.cuda.Stream(), torch.cuda.Stream()
-    e = Emulation(w, stream=compute)
-    with torch.cuda.stream(compute):
-        e.init_params()
-        e.fill_grads(1)
+    if WORKLOADS[args.workload][1] is not None:
+        raise SystemExit("--coordinator needs a full emulation workload")
+    w, e, compute, desc = setup_single(args, bucketed=False)
+    prefetch = torch.cuda.Stream()
     plan = e.plan
     n_sub = plan.info.n_submodules
     sizes = [plan.submodule(k)[1] for k in range(n_sub)]
@@ -433,21 +439,12 @@ def run_qwz(args):
     """The qwZ step: fused reduce-scatter + AdamW + bf16 shard + int8 block
     quantization, then the dequantizing all-gather into the full buffer."""
     import torch
-    from zero_sharded_optimizer_shard_gb300 import build as b
-    b.build_all(quiet=True)
     from zero_sharded_optimizer_shard_gb300 import zero3
-    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
-    torch.cuda.set_device(0)
-    fac, state_ranks, bucketed, desc = WORKLOADS[args.workload]
-    if state_ranks is not None:
+    if WORKLOADS[args.workload][1] is not None:
         raise SystemExit("--qwz needs a full emulation workload")
-    w = make_workload(args)
-    stream = torch.cuda.Stream()
-    e = Emulation(w, stream=stream)
+    w, e, stream, desc = setup_single(args, bucketed=False)
     nb = -(-e.S // 256)
     with torch.cuda.stream(stream):
-        e.init_params()
-        e.fill_grads(1)
         codes = [torch.empty(e.S, dtype=torch.int8, device="cuda") for _ in range(e.nd)]
         scales = [torch.empty(nb, dtype=torch.float32, device="cuda") for _ in range(e.nd)]
     torch.cuda.synchronize()
@@ -513,17 +510,11 @@ def run_qwz(args):
 def run_unfused(args):
     """Ablation: the same step as three launches (what fusion saves)."""
     import torch
-    from zero_sharded_optimizer_shard_gb300 import build as b
-    b.build_all(quiet=True)
     from zero_sharded_optimizer_shard_gb300 import zero3
-    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
-    torch.cuda.set_device(0)
-    w = make_workload(args)
-    stream = torch.cuda.Stream()
-    e = Emulation(w, stream=stream)
+    if WORKLOADS[args.workload][1] is not None:
+        raise SystemExit("--unfused needs a full emulation workload")
+    w, e, stream, desc = setup_single(args, bucketed=False)
     with torch.cuda.stream(stream):
-        e.init_params()
-        e.fill_grads(1)
         sg = [torch.empty(e.S, dtype=torch.float32, device="cuda") for _ in range(e.nd)]
     torch.cuda.synchronize()
     lo, hi = e.chunks[0]

@@ -62,8 +62,6 @@ struct RankPtrs {
     float* const* v = nullptr;
     void* const* out = nullptr;        // sparam or shard grad
     const void* const* in = nullptr;   // shard grad, sparam or master
-    int out_elem = 2;                  // bytes per element of out
-    int in_elem = 0;                   // bytes per element of in (0: unused)
     uint16_t* full = nullptr;
     int8_t* const* codes = nullptr;    // qwZ codes per rank
     float* const* scales = nullptr;    // qwZ scales per rank

@@ -66,6 +66,7 @@ def parse():
     ap.add_argument("--qwz", action="store_true",
                     help="ZeRO++ qwZ: the fused step emits int8 codes + block scales and the "
                          "all-gather dequantizes them into the full buffer")
+    ap.add_argument("--qwz-bits", type=int, choices=[8, 4], default=8)
     ap.add_argument("--unfused", action="store_true",
                     help="ablation: reduce-scatter (fp32 shard gradient), AdamW and all-gather "
                          "as three launches, each timed")
@@ -445,7 +446,8 @@ def run_qwz(args):
     w, e, stream, desc = setup_single(args, bucketed=False)
     nb = -(-e.S // 256)
     with torch.cuda.stream(stream):
-        codes = [torch.empty(e.S, dtype=torch.int8, device="cuda") for _ in range(e.nd)]
+        codes = [torch.empty(-(-e.S * args.qwz_bits // 8), dtype=torch.int8, device="cuda")
+                 for _ in range(e.nd)]
         scales = [torch.empty(nb, dtype=torch.float32, device="cuda") for _ in range(e.nd)]
     torch.cuda.synchronize()
     cp, sp = e.ptrs(codes), e.ptrs(scales)
@@ -456,9 +458,11 @@ def run_qwz(args):
         a0, a1, a2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         a0.record(stream)
         zero3.zero3_step_qwz(e.plan, e.hp, t, e.ptrs(e.grads[0]), lo, e.ptrs(e.master), e.ptrs(e.m),
-                             e.ptrs(e.v), e.ptrs(e.sparam), cp, sp, None, lo, hi, e.sid)
+                             e.ptrs(e.v), e.ptrs(e.sparam), cp, sp, None, lo, hi, e.sid,
+                             bits=args.qwz_bits)
         a1.record(stream)
-        zero3.zero3_allgather_qwz(e.plan, cp, sp, e.full.data_ptr(), lo, hi, e.sid)
+        zero3.zero3_allgather_qwz(e.plan, cp, sp, e.full.data_ptr(), lo, hi, e.sid,
+                                  bits=args.qwz_bits)
         a2.record(stream)
         zero3.zero3_persistent_step(e.plan, e.hp, t, e.persist, e.sid)
         if timed:
@@ -486,15 +490,17 @@ def run_qwz(args):
     fused_ms = statistics.mean(a.elapsed_time(b_) for a, b_, _ in ev)
     gather_ms = statistics.mean(b_.elapsed_time(c) for _, b_, c in ev)
     n = hi - lo
-    fused_bytes = n * (2 * w.n_ranks + 24 + 2 + 1) + e.nd * nb * 4
-    gather_bytes = n * (1 + 2) + e.nd * nb * 4
+    cb = args.qwz_bits / 8
+    fused_bytes = n * (2 * w.n_ranks + 24 + 2 + cb) + e.nd * nb * 4
+    gather_bytes = n * (cb + 2) + e.nd * nb * 4
     peak, peak_kind = peaks()
     ach = fused_bytes / (fused_ms / 1e3) / 1e9
     print(json.dumps({
         "metric": METRIC, "value": w.psi / (ms / 1e3), "unit": "params/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": desc + ", qwZ int8 all-gather (block 256)", "name": args.workload,
+        "config": {"workload": desc + f", qwZ int{args.qwz_bits} all-gather (block 256)",
+                   "name": args.workload,
                    "n_ranks": w.n_ranks, "params": w.psi},
         "fused_qwz": {"ms_per_launch": fused_ms, "bytes_per_launch": fused_bytes,
                       "gbs": ach, "frac": ach / peak},

@@ -240,17 +240,20 @@ zero3_status zero3_step_stage12(const zero3_plan* plan, const zero3_adamw_hparam
                                 zero3_stream stream);
 
 /* ----------------------------------------------------- qwZ (ZeRO++)
- * The parameter all-gather sends int8 codes instead of bf16 values
+ * The parameter all-gather sends int8 or int4 codes instead of bf16 values
  * ([compass] section ZeRO++: qwZ quantizes the weights of the all-gather to
  * int8/int4 to cut the communicated volume).  The pages give no block size
- * or scale format; this library fixes: symmetric int8, one fp32 scale per
- * ZERO3_QWZ_BLOCK = 256 consecutive elements of a rank's shard (local
- * indices [256b, 256b+256); a shard's last block may be shorter),
- *   absmax = max |x|, x = f32(bf16 parameter);  scale = absmax / 127;
- *   code = round-half-even(x * (127 / absmax)), 0 when absmax = 0;
+ * or scale format; this library fixes: symmetric integers of `bits` = 8 or 4
+ * bits (qmax = 127 or 7), one fp32 scale per ZERO3_QWZ_BLOCK = 256
+ * consecutive elements of a rank's shard (local indices [256b, 256b+256); a
+ * shard's last block may be shorter),
+ *   absmax = max |x|, x = f32(bf16 parameter);  scale = absmax / qmax;
+ *   code = round-half-even(x * (qmax / absmax)), 0 when absmax = 0;
  * and the receiver writes bf16_rne(code * scale).  Layout per rank r:
- * codes[r] int8 [S], scales[r] fp32 [ceil(S/256)] (host arrays of N_d device
- * pointers, 16-byte aligned).  Quantizing calls need ranges that cover whole
+ * codes[r] [ceil(S * bits / 8)] bytes (int8: one byte per element; int4: two
+ * per byte, element 2j in the low nibble, two's complement), scales[r] fp32
+ * [ceil(S/256)] (host arrays of N_d device pointers, 16-byte aligned).  Any
+ * other `bits` is ZERO3_EINVAL.  Quantizing calls need ranges that cover whole
  * blocks of every shard they touch: each rank's local range must start on a
  * multiple of 256 and end on one or at S (else ZERO3_EINVAL). */
 #define ZERO3_QWZ_BLOCK 256
@@ -261,18 +264,18 @@ zero3_status zero3_step_stage12(const zero3_plan* plan, const zero3_adamw_hparam
 zero3_status zero3_step_qwz(const zero3_plan* plan, const zero3_adamw_hparams* hp, int64_t t,
                             const uint16_t* const* grads, int64_t grads_origin,
                             float* const* master, float* const* m, float* const* v,
-                            uint16_t* const* sparam, int8_t* const* codes, float* const* scales,
-                            const zero3_persist_state* persist, int64_t flat_lo,
-                            int64_t flat_hi, zero3_stream stream);
+                            uint16_t* const* sparam, int32_t bits, int8_t* const* codes,
+                            float* const* scales, const zero3_persist_state* persist,
+                            int64_t flat_lo, int64_t flat_hi, zero3_stream stream);
 
 /* Quantizes existing bf16 shards into codes/scales (e.g. at initialisation). */
 zero3_status zero3_quantize_shards(const zero3_plan* plan, const uint16_t* const* sparam,
-                                   int8_t* const* codes, float* const* scales, int64_t flat_lo,
-                                   int64_t flat_hi, zero3_stream stream);
+                                   int32_t bits, int8_t* const* codes, float* const* scales,
+                                   int64_t flat_lo, int64_t flat_hi, zero3_stream stream);
 
-/* The quantized all-gather: full[r*S + i] = bf16_rne(codes[r][i] *
+/* The quantized all-gather: full[r*S + i] = bf16_rne(code_r(i) *
  * scales[r][i / 256]) for every flat index in the range (any range). */
-zero3_status zero3_allgather_qwz(const zero3_plan* plan, const int8_t* const* codes,
+zero3_status zero3_allgather_qwz(const zero3_plan* plan, int32_t bits, const int8_t* const* codes,
                                  const float* const* scales, uint16_t* full, int64_t flat_lo,
                                  int64_t flat_hi, zero3_stream stream);
 

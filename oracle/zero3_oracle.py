@@ -450,19 +450,22 @@ def ddp_step(plan: Plan, hp: dict, t: int, grads: Sequence[np.ndarray], st: DDPS
 QWZ_BLOCK = 256
 
 
-def qwz_quantize(param_bf16: np.ndarray, block: int = QWZ_BLOCK):
+def qwz_quantize(param_bf16: np.ndarray, block: int = QWZ_BLOCK, bits: int = 8):
     """Quantize one rank's 2-byte parameter shard for the all-gather.
 
     ZeRO++'s qwZ sends the weights of the parameter all-gather quantized to
-    int8 (or int4) to cut the communicated volume (ZeRO concept page,
-    section ZeRO++).  The pages give no block size or scale format; reading
-    taken: symmetric int8, one binary32 scale per `block` consecutive
-    elements of the shard (the last block may be shorter):
+    int8 or int4 to cut the communicated volume (ZeRO concept page, section
+    ZeRO++).  The pages give no block size or scale format; reading taken:
+    symmetric integers with qmax = 2**(bits-1) - 1 (127 or 7), one binary32
+    scale per `block` consecutive elements of the shard (the last block may
+    be shorter):
         absmax = max |x| over the block (x = f32(bf16 param), exact)
-        scale  = absmax / 127                      (one binary32 division)
-        inv    = 127 / absmax, or 0 when absmax = 0 (one binary32 division)
-        code   = round_half_even(x * inv)          (one binary32 product)
-    Returns (int8 codes, binary32 scales)."""
+        scale  = absmax / qmax                      (one binary32 division)
+        inv    = qmax / absmax, or 0 when absmax = 0 (one binary32 division)
+        code   = round_half_even(x * inv)           (one binary32 product)
+    Returns (codes as int8 values, binary32 scales); qwz_pack gives the
+    transmitted bytes."""
+    qmax = np.float32(2 ** (bits - 1) - 1)
     x = bf16_to_f32(param_bf16)
     n = x.size
     nb = -(-n // block)
@@ -471,10 +474,33 @@ def qwz_quantize(param_bf16: np.ndarray, block: int = QWZ_BLOCK):
     for b in range(nb):
         xb = x[b * block:(b + 1) * block]
         amax = np.max(np.abs(xb)) if xb.size else F32(0)
-        scales[b] = F32(amax) / F32(127.0)
-        inv = (F32(127.0) / F32(amax)) if amax > 0 else F32(0.0)
-        codes[b * block:(b + 1) * block] = np.clip(np.rint(xb * inv), -127, 127).astype(np.int8)
+        scales[b] = F32(amax) / qmax
+        inv = (qmax / F32(amax)) if amax > 0 else F32(0.0)
+        codes[b * block:(b + 1) * block] = np.clip(np.rint(xb * inv), -qmax, qmax).astype(np.int8)
     return codes, scales
+
+
+def qwz_pack(codes: np.ndarray, bits: int = 8) -> np.ndarray:
+    """Transmitted bytes: int8 codes as they are; int4 codes two per byte,
+    element 2j in the low nibble and 2j+1 in the high nibble (two's
+    complement nibbles; an odd tail leaves the high nibble zero)."""
+    if bits == 8:
+        return codes.view(np.uint8).copy()
+    c = (codes.astype(np.int16) & 0xF).astype(np.uint8)
+    if c.size % 2:
+        c = np.concatenate([c, np.zeros(1, np.uint8)])
+    return (c[0::2] | (c[1::2] << 4)).astype(np.uint8)
+
+
+def qwz_unpack(packed: np.ndarray, n: int, bits: int = 8) -> np.ndarray:
+    if bits == 8:
+        return np.asarray(packed, np.uint8)[:n].view(np.int8)
+    p = np.asarray(packed, np.uint8)
+    nib = np.empty(p.size * 2, np.int16)
+    nib[0::2] = p & 0xF
+    nib[1::2] = p >> 4
+    nib = np.where(nib >= 8, nib - 16, nib)
+    return nib[:n].astype(np.int8)
 
 
 def qwz_dequantize(codes: np.ndarray, scales: np.ndarray, block: int = QWZ_BLOCK) -> np.ndarray:

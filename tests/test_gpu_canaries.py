@@ -65,11 +65,16 @@ def test_every_writer_stays_in_bounds(wname, tmp_path):
     nb = -(-S // 256)
     codes = [q.alloc(S, torch.int8) for _ in range(nd)]
     scales = [q.alloc(nb, torch.float32) for _ in range(nd)]
-    zero3.zero3_step_qwz(q.plan, q.hp, 1, P(q.grads[0]), 0, P(q.master), P(q.m), P(q.v),
-                         P(q.sparam), P(codes), P(scales), q.persist, 0, q.psi_pad, q.sid)
-    zero3.zero3_quantize_shards(q.plan, P(q.sparam), P(codes), P(scales), 0, q.psi_pad, q.sid)
-    zero3.zero3_allgather_qwz(q.plan, P(codes), P(scales), q.full.data_ptr(), 0, q.psi_pad, q.sid)
-    ok(q, "qwZ")
+    for bits in (8, 4):
+        cb = [q.alloc(-(-S * bits // 8), torch.int8) for _ in range(nd)]
+        zero3.zero3_step_qwz(q.plan, q.hp, 1, P(q.grads[0]), 0, P(q.master), P(q.m), P(q.v),
+                             P(q.sparam), P(cb), P(scales), q.persist, 0, q.psi_pad, q.sid,
+                             bits=bits)
+        zero3.zero3_quantize_shards(q.plan, P(q.sparam), P(cb), P(scales), 0, q.psi_pad, q.sid,
+                                    bits=bits)
+        zero3.zero3_allgather_qwz(q.plan, P(cb), P(scales), q.full.data_ptr(), 0, q.psi_pad,
+                                  q.sid, bits=bits)
+        ok(q, f"qwZ int{bits}")
     del q, codes, scales
     # checkpoint round trip writes the states back through host staging
     for r in range(nd):

@@ -7,7 +7,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import oracle as O  # noqa: E402
-from tests._oracle_runs import bits, f32, host_grads, host_master, u16  # noqa: E402
+from tests._oracle_runs import bits as b32, f32, host_grads, host_master, u16  # noqa: E402
 from zero_sharded_optimizer_shard_gb300 import workloads as W  # noqa: E402
 
 pytestmark = pytest.mark.gpu
@@ -24,8 +24,9 @@ def i8(t):
     return t.detach().cpu().numpy().view(np.int8)
 
 
+@pytest.mark.parametrize("bits", [8, 4])
 @pytest.mark.parametrize("wname", ["mini2", "mini3", "mini8", "ragged7"])
-def test_qwz_step_and_allgather_match_oracle(wname):
+def test_qwz_step_and_allgather_match_oracle(wname, bits):
     from zero_sharded_optimizer_shard_gb300 import zero3
     from zero_sharded_optimizer_shard_gb300.emulation import Emulation
     w = {"mini2": lambda: W.mini_gpt(2), "mini3": lambda: W.mini_gpt(3),
@@ -40,17 +41,19 @@ def test_qwz_step_and_allgather_match_oracle(wname):
         e.fill_grads(t)
         zero3.zero3_step_qwz(e.plan, e.hp, t, e.ptrs(e.grads[0]), 0, e.ptrs(e.master), e.ptrs(e.m),
                              e.ptrs(e.v), e.ptrs(e.sparam), e.ptrs(codes), e.ptrs(scales), None,
-                             0, e.psi_pad, e.sid)
+                             0, e.psi_pad, e.sid, bits=bits)
         zero3.zero3_allgather_qwz(e.plan, e.ptrs(codes), e.ptrs(scales), e.full.data_ptr(), 0,
-                                  e.psi_pad, e.sid)
+                                  e.psi_pad, e.sid, bits=bits)
         O.sharded_step(plan, w.hparams, t, host_grads(w, plan, t), st, full)
     torch.cuda.synchronize()
-    q = [O.qwz_quantize(st.sparam[r]) for r in range(w.n_ranks)]
+    q = [O.qwz_quantize(st.sparam[r], bits=bits) for r in range(w.n_ranks)]
+    nbytes = -(-e.S * bits // 8)
     for r in range(w.n_ranks):
-        assert np.array_equal(bits(f32(e.master[r])), bits(st.master[r]))
+        assert np.array_equal(b32(f32(e.master[r])), b32(st.master[r]))
         assert np.array_equal(u16(e.sparam[r]), st.sparam[r])
-        assert np.array_equal(i8(codes[r])[:e.S], q[r][0]), f"codes rank {r}"
-        assert np.array_equal(bits(f32(scales[r])[:q[r][1].size]), bits(q[r][1])), f"scales {r}"
+        wire_bytes = i8(codes[r])[:nbytes].view(np.uint8)
+        assert np.array_equal(wire_bytes, O.qwz_pack(q[r][0], bits)), f"codes rank {r}"
+        assert np.array_equal(b32(f32(scales[r])[:q[r][1].size]), b32(q[r][1])), f"scales {r}"
     want = O.qwz_allgather(plan, [c for c, _ in q], [s for _, s in q])
     assert np.array_equal(u16(e.full), want)
 
@@ -72,7 +75,7 @@ def test_quantize_shards_and_partial_ranges():
     for r in range(3):
         c, s = O.qwz_quantize(u16(e.sparam[r]))
         assert np.array_equal(i8(codes[r])[:S], c)
-        assert np.array_equal(bits(f32(scales[r])[:s.size]), bits(s))
+        assert np.array_equal(b32(f32(scales[r])[:s.size]), b32(s))
     # sub-range: rank 1's blocks 2..5 only
     for x in codes:
         x.zero_()
@@ -104,3 +107,16 @@ def test_quantize_shards_and_partial_ranges():
     assert np.array_equal(got[lo:S], O.qwz_dequantize(c0, s0)[lo:S])
     assert np.array_equal(got[S:2 * S], O.qwz_dequantize(c1, s1))
     assert np.array_equal(got[2 * S:hi], O.qwz_dequantize(c2, s2)[:hi - 2 * S])
+
+
+def test_qwz_rejects_other_widths():
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+    e = Emulation(W.toy_mlp())
+    e.init_params()
+    codes, scales = wire(e)
+    for b in (0, 2, 16):
+        with pytest.raises(zero3.Zero3Error) as exc:
+            zero3.zero3_quantize_shards(e.plan, e.ptrs(e.sparam), e.ptrs(codes), e.ptrs(scales), 0,
+                                        e.psi_pad, e.sid, bits=b)
+        assert exc.value.status == zero3.EINVAL

@@ -485,3 +485,29 @@ def test_plan_memory_reduces_to_closed_form():
     plan = O.partition([1001, 50], None, 4, threshold=100)
     assert plan.psi_pad == 1004 and plan.psi_s == 50
     assert O.plan_memory_bytes(plan, 3) == 16 * 1004 / 4 + 16 * 50
+
+
+def test_qwz_int4_hand_example():
+    g = golden("qwz_int4_block_example.json")
+    codes, scales = O.qwz_quantize(bf16(g["x"]), block=g["block"], bits=4)
+    assert list(codes) == g["codes"]
+    assert list(O.qwz_pack(codes, bits=4)) == g["packed"]
+    assert list(O.qwz_unpack(O.qwz_pack(codes, bits=4), len(codes), bits=4)) == g["codes"]
+    deq = O.bf16_to_f32(O.qwz_dequantize(codes, scales, block=g["block"]))
+    assert list(map(float, deq)) == g["dequant"]
+
+
+def test_qwz_int4_error_bound():
+    rng = np.random.default_rng(22)
+    x16 = bf16((rng.standard_normal(5_000) * 0.02).astype(np.float32))
+    codes, scales = O.qwz_quantize(x16, bits=4)
+    assert np.abs(codes.astype(int)).max() <= 7
+    x = O.bf16_to_f32(x16).astype(np.float64)
+    y = O.bf16_to_f32(O.qwz_dequantize(codes, scales)).astype(np.float64)
+    s = np.repeat(scales.astype(np.float64), 256)[:x.size]
+    assert np.all(np.abs(y - x) <= s / 2 * (1 + 1e-6) + np.abs(x) * 2.0 ** -8 + 1e-45)
+    # pack/unpack round trip for both widths, odd and even lengths
+    for bits in (8, 4):
+        for n in (5_000, 4_999):
+            c = codes[:n]
+            assert np.array_equal(O.qwz_unpack(O.qwz_pack(c, bits), n, bits), c)

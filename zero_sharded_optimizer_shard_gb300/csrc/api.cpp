@@ -360,11 +360,12 @@ zero3_status zero3_step_stage12(const zero3_plan* p, const zero3_adamw_hparams* 
 zero3_status zero3_step_qwz(const zero3_plan* p, const zero3_adamw_hparams* hp, int64_t t,
                             const uint16_t* const* grads, int64_t grads_origin,
                             float* const* master, float* const* m, float* const* v,
-                            uint16_t* const* sparam, int8_t* const* codes,
+                            uint16_t* const* sparam, int32_t bits, int8_t* const* codes,
                             float* const* scales, const zero3_persist_state* persist,
                             int64_t lo, int64_t hi, zero3_stream stream) {
     if (!p || !range_ok(p, lo, hi) || !hparams_ok(hp, t) || grads_origin > lo)
         return ZERO3_EINVAL;
+    if (bits != 8 && bits != 4) return ZERO3_EINVAL;
     const z3::Scalars sc = step_scalars(p, hp, t);
     if (lo < hi) {
         if (!grads_ok(p, grads) || !sparam || !codes || !scales) return ZERO3_EINVAL;
@@ -380,7 +381,7 @@ zero3_status zero3_step_qwz(const zero3_plan* p, const zero3_adamw_hparams* hp, 
         rp.scales = scales;
         rp.warp_blocks = true;
         StreamArgs a;
-        zero3_status st = build_args(p, z3::kFusedQ, rp, lo, hi, &sc, 0, a);
+        zero3_status st = build_args(p, z3::kFusedQ, rp, lo, hi, &sc, bits, a);
         if (st != ZERO3_OK) return st;
         if (persist && !persist_ok(p, persist)) return ZERO3_EINVAL;
         st = cuda_status(z3::launch_stream(z3::kFusedQ, a, stream));
@@ -391,9 +392,10 @@ zero3_status zero3_step_qwz(const zero3_plan* p, const zero3_adamw_hparams* hp, 
 }
 
 zero3_status zero3_quantize_shards(const zero3_plan* p, const uint16_t* const* sparam,
-                                   int8_t* const* codes, float* const* scales, int64_t lo,
-                                   int64_t hi, zero3_stream stream) {
+                                   int32_t bits, int8_t* const* codes, float* const* scales,
+                                   int64_t lo, int64_t hi, zero3_stream stream) {
     if (!p || !range_ok(p, lo, hi)) return ZERO3_EINVAL;
+    if (bits != 8 && bits != 4) return ZERO3_EINVAL;
     if (lo == hi) return ZERO3_OK;
     if (!sparam || !codes || !scales) return ZERO3_EINVAL;
     RankPtrs rp;
@@ -402,15 +404,16 @@ zero3_status zero3_quantize_shards(const zero3_plan* p, const uint16_t* const* s
     rp.scales = scales;
     rp.warp_blocks = true;
     StreamArgs a;
-    zero3_status st = build_args(p, z3::kQuant, rp, lo, hi, nullptr, 0, a);
+    zero3_status st = build_args(p, z3::kQuant, rp, lo, hi, nullptr, bits, a);
     if (st != ZERO3_OK) return st;
     return cuda_status(z3::launch_stream(z3::kQuant, a, stream));
 }
 
-zero3_status zero3_allgather_qwz(const zero3_plan* p, const int8_t* const* codes,
+zero3_status zero3_allgather_qwz(const zero3_plan* p, int32_t bits, const int8_t* const* codes,
                                  const float* const* scales, uint16_t* full, int64_t lo,
                                  int64_t hi, zero3_stream stream) {
     if (!p || !range_ok(p, lo, hi)) return ZERO3_EINVAL;
+    if (bits != 8 && bits != 4) return ZERO3_EINVAL;
     if (lo == hi) return ZERO3_OK;
     if (!codes || !scales || !full || !aligned16(full)) return ZERO3_EINVAL;
     RankPtrs rp;
@@ -418,7 +421,7 @@ zero3_status zero3_allgather_qwz(const zero3_plan* p, const int8_t* const* codes
     rp.codes = const_cast<int8_t* const*>(codes);
     rp.scales = const_cast<float* const*>(scales);
     StreamArgs a;
-    zero3_status st = build_args(p, z3::kDequant, rp, lo, hi, nullptr, 0, a);
+    zero3_status st = build_args(p, z3::kDequant, rp, lo, hi, nullptr, bits, a);
     if (st != ZERO3_OK) return st;
     return cuda_status(z3::launch_stream(z3::kDequant, a, stream));
 }

@@ -83,7 +83,7 @@ struct StreamArgs {
     int64_t total_chunks;
     int32_t n_spans;
     int32_t nd;
-    int32_t dtype;       // zero3_dtype of the shard grad (kReduce out / kAdam in)
+    int32_t dtype;       // zero3_dtype of the shard grad (kReduce out / kAdam in); qwZ bits
     int32_t pad_;
     Scalars sc;
 };

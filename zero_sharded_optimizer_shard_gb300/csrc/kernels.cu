@@ -146,14 +146,25 @@ __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp
         return;
     }
     if constexpr (MODE == kDequant) {
-        const uint2 q = __ldcs(reinterpret_cast<const uint2*>(sp.codes + i0));
         const float sc = sp.scales[i0 / kQwzBlock];
         float y[8];
+        if constexpr (GT == 4) {
+            // 8 two's-complement nibbles, element i0+e in bits 4e..4e+3
+            const uint32_t w = __ldcs(reinterpret_cast<const unsigned int*>(
+                reinterpret_cast<const uint8_t*>(sp.codes) + i0 / 2));
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const uint32_t w = e < 4 ? q.x : q.y;
-            const int8_t c = static_cast<int8_t>((w >> (8 * (e & 3))) & 0xffu);
-            y[e] = __fmul_rn(static_cast<float>(c), sc);
+            for (int e = 0; e < 8; ++e) {
+                const int c = static_cast<int>(w << (28 - 4 * e)) >> 28;
+                y[e] = __fmul_rn(static_cast<float>(c), sc);
+            }
+        } else {
+            const uint2 q = __ldcs(reinterpret_cast<const uint2*>(sp.codes + i0));
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t w = e < 4 ? q.x : q.y;
+                const int8_t c = static_cast<int8_t>((w >> (8 * (e & 3))) & 0xffu);
+                y[e] = __fmul_rn(static_cast<float>(c), sc);
+            }
         }
         stcs16(a.full + sp.fofs + i0, pack8(y));
         return;
@@ -238,7 +249,14 @@ __device__ __forceinline__ void scalar_chunk(const StreamArgs& a, const Span& sp
             continue;
         }
         if constexpr (MODE == kDequant) {
-            const float y = __fmul_rn(static_cast<float>(sp.codes[i]), sp.scales[i / kQwzBlock]);
+            int c;
+            if constexpr (GT == 4) {
+                const uint32_t b = reinterpret_cast<const uint8_t*>(sp.codes)[i / 2];
+                c = static_cast<int>(b << (28 - 4 * (i & 1))) >> 28;  // sign-extend the nibble
+            } else {
+                c = sp.codes[i];
+            }
+            const float y = __fmul_rn(static_cast<float>(c), sp.scales[i / kQwzBlock]);
             a.full[sp.fofs + i] = to_bf16(y);
             continue;
         }
@@ -286,30 +304,48 @@ __device__ __forceinline__ void scalar_chunk(const StreamArgs& a, const Span& sp
 }
 
 // qwZ epilogue: the warp's 32 chunks are one 256-element block of one shard
-// (the launch numbers chunks that way).  absmax by warp shuffle, then
-// scale = absmax/127, code = round-half-even(x * 127/absmax), one binary32
-// operation each.  Every lane of the warp reaches the shuffles.
+// (the launch numbers chunks that way).  absmax by warp shuffle, then with
+// qmax = 2^(BITS-1) - 1: scale = absmax/qmax, code = round-half-even(x *
+// qmax/absmax), one binary32 operation each.  int8 codes take a byte each;
+// int4 codes two per byte, element 2j in the low nibble.  Every lane of the
+// warp reaches the shuffles.
+template <int BITS>
 __device__ __forceinline__ void qwz_block(const Span& sp, int64_t i0, const float* hq) {
+    constexpr float kQmax = BITS == 4 ? 7.0f : 127.0f;
+    constexpr int kQi = BITS == 4 ? 7 : 127;
     float am = 0.0f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(hq[e]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    const float inv = am > 0.0f ? __fdiv_rn(127.0f, am) : 0.0f;
+    const float inv = am > 0.0f ? __fdiv_rn(kQmax, am) : 0.0f;
     uint32_t w[2] = {0u, 0u};
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         int q = __float2int_rn(__fmul_rn(hq[e], inv));
-        q = q > 127 ? 127 : (q < -127 ? -127 : q);
-        w[e >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << (8 * (e & 3));
+        q = q > kQi ? kQi : (q < -kQi ? -kQi : q);
+        if constexpr (BITS == 4)
+            w[0] |= (static_cast<uint32_t>(q) & 0xfu) << (4 * e);
+        else
+            w[e >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << (8 * (e & 3));
     }
     if (i0 >= sp.hi) return;  // chunk past the shard's end: nothing to store
-    if ((threadIdx.x & 31) == 0) sp.scales[i0 / kQwzBlock] = __fdiv_rn(am, 127.0f);
-    if (i0 + 8 <= sp.hi) {
-        *reinterpret_cast<uint2*>(sp.codes + i0) = make_uint2(w[0], w[1]);
+    if ((threadIdx.x & 31) == 0) sp.scales[i0 / kQwzBlock] = __fdiv_rn(am, kQmax);
+    uint8_t* bytes = reinterpret_cast<uint8_t*>(sp.codes);
+    if constexpr (BITS == 4) {
+        if (i0 + 8 <= sp.hi) {
+            *reinterpret_cast<uint32_t*>(bytes + i0 / 2) = w[0];
+        } else {  // shard end: ceil((hi - i0) / 2) bytes, unused nibbles are 0
+            for (int b = 0; 2 * b < sp.hi - i0; ++b)
+                bytes[i0 / 2 + b] = static_cast<uint8_t>((w[0] >> (8 * b)) & 0xffu);
+        }
     } else {
-        for (int e = 0; e < 8 && i0 + e < sp.hi; ++e)
-            sp.codes[i0 + e] = static_cast<int8_t>((w[e >> 2] >> (8 * (e & 3))) & 0xffu);
+        if (i0 + 8 <= sp.hi) {
+            *reinterpret_cast<uint2*>(bytes + i0) = make_uint2(w[0], w[1]);
+        } else {
+            for (int e = 0; e < 8 && i0 + e < sp.hi; ++e)
+                bytes[i0 + e] = static_cast<uint8_t>((w[e >> 2] >> (8 * (e & 3))) & 0xffu);
+        }
     }
 }
 
@@ -344,7 +380,7 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const __grid_constant_
                 vector_chunk<MODE, ND, GT>(a, sp, i0, hq);
             else
                 scalar_chunk<MODE, ND, GT>(a, sp, i0, hq);
-            if constexpr (MODE == kFusedQ || MODE == kQuant) qwz_block(sp, i0, hq);
+            if constexpr (MODE == kFusedQ || MODE == kQuant) qwz_block<GT == 4 ? 4 : 8>(sp, i0, hq);
         }
     }
 }
@@ -412,9 +448,15 @@ cudaError_t launch_stream(int mode, const StreamArgs& a, cudaStream_t stream) {
     switch (mode) {
         case kFused: return launch_nd<kFused, 0>(a, stream);
         case kFusedRep: return launch_nd<kFusedRep, 0>(a, stream);
-        case kFusedQ: return launch_nd<kFusedQ, 0>(a, stream);
-        case kQuant: return launch_one<kQuant, 1, 0>(a, stream);
-        case kDequant: return launch_one<kDequant, 1, 0>(a, stream);
+        // qwZ modes: the template's GT carries the code width (8 or 4 bits)
+        case kFusedQ:
+            return a.dtype == 4 ? launch_nd<kFusedQ, 4>(a, stream) : launch_nd<kFusedQ, 8>(a, stream);
+        case kQuant:
+            return a.dtype == 4 ? launch_one<kQuant, 1, 4>(a, stream)
+                                : launch_one<kQuant, 1, 8>(a, stream);
+        case kDequant:
+            return a.dtype == 4 ? launch_one<kDequant, 1, 4>(a, stream)
+                                : launch_one<kDequant, 1, 8>(a, stream);
         case kReduce:
             return a.dtype == ZERO3_BF16 ? launch_nd<kReduce, ZERO3_BF16>(a, stream)
                                          : launch_nd<kReduce, ZERO3_F32>(a, stream);

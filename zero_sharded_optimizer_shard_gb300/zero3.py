@@ -102,12 +102,12 @@ _SIGS = [
                                      C.POINTER(_vp), C.c_int64, C.c_int64, _vp]),
     ("zero3_step_qwz", C.c_int, [_vp, C.POINTER(AdamWHparams), C.c_int64, C.POINTER(_vp),
                                  C.c_int64, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp),
-                                 C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp),
+                                 C.POINTER(_vp), C.c_int32, C.POINTER(_vp), C.POINTER(_vp),
                                  C.POINTER(PersistState), C.c_int64, C.c_int64, _vp]),
-    ("zero3_quantize_shards", C.c_int, [_vp, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp),
-                                        C.c_int64, C.c_int64, _vp]),
-    ("zero3_allgather_qwz", C.c_int, [_vp, C.POINTER(_vp), C.POINTER(_vp), _vp, C.c_int64,
-                                      C.c_int64, _vp]),
+    ("zero3_quantize_shards", C.c_int, [_vp, C.POINTER(_vp), C.c_int32, C.POINTER(_vp),
+                                        C.POINTER(_vp), C.c_int64, C.c_int64, _vp]),
+    ("zero3_allgather_qwz", C.c_int, [_vp, C.c_int32, C.POINTER(_vp), C.POINTER(_vp), _vp,
+                                      C.c_int64, C.c_int64, _vp]),
     ("zero3_persistent_step", C.c_int, [_vp, C.POINTER(AdamWHparams), C.c_int64,
                                         C.POINTER(PersistState), _vp]),
     ("zero3_cast_params", C.c_int, [_vp, C.POINTER(_vp), C.POINTER(_vp), _vp,
@@ -278,21 +278,22 @@ QWZ_BLOCK = 256
 
 
 def zero3_step_qwz(plan: Plan, hp, t, grads, grads_origin, master, m, v, sparam, codes, scales,
-                   persist, flat_lo, flat_hi, stream=0):
+                   persist, flat_lo, flat_hi, stream=0, bits=8):
     _check(plan._lib.zero3_step_qwz(plan.handle, C.byref(hp), t, _ptrs(grads), grads_origin,
-                                    _ptrs(master), _ptrs(m), _ptrs(v), _ptrs(sparam), _ptrs(codes),
-                                    _ptrs(scales), _ps_ref(persist), flat_lo, flat_hi, stream),
-           "zero3_step_qwz")
+                                    _ptrs(master), _ptrs(m), _ptrs(v), _ptrs(sparam), bits,
+                                    _ptrs(codes), _ptrs(scales), _ps_ref(persist), flat_lo,
+                                    flat_hi, stream), "zero3_step_qwz")
 
 
-def zero3_quantize_shards(plan: Plan, sparam, codes, scales, flat_lo, flat_hi, stream=0):
-    _check(plan._lib.zero3_quantize_shards(plan.handle, _ptrs(sparam), _ptrs(codes), _ptrs(scales),
-                                           flat_lo, flat_hi, stream), "zero3_quantize_shards")
+def zero3_quantize_shards(plan: Plan, sparam, codes, scales, flat_lo, flat_hi, stream=0, bits=8):
+    _check(plan._lib.zero3_quantize_shards(plan.handle, _ptrs(sparam), bits, _ptrs(codes),
+                                           _ptrs(scales), flat_lo, flat_hi, stream),
+           "zero3_quantize_shards")
 
 
-def zero3_allgather_qwz(plan: Plan, codes, scales, full, flat_lo, flat_hi, stream=0):
-    _check(plan._lib.zero3_allgather_qwz(plan.handle, _ptrs(codes), _ptrs(scales), full, flat_lo,
-                                         flat_hi, stream), "zero3_allgather_qwz")
+def zero3_allgather_qwz(plan: Plan, codes, scales, full, flat_lo, flat_hi, stream=0, bits=8):
+    _check(plan._lib.zero3_allgather_qwz(plan.handle, bits, _ptrs(codes), _ptrs(scales), full,
+                                         flat_lo, flat_hi, stream), "zero3_allgather_qwz")
 
 
 def zero3_persistent_step(plan: Plan, hp, t, persist, stream=0):

@@ -37,6 +37,8 @@ WORKLOADS = {
                      "full emulation in one HBM"),
     "gpt2_small": ("gpt2_small", None, False,
                    "GPT-2-small list (12L, d=768, vocab 50257), N_d=4 virtual ranks"),
+    "ragged": ("ragged", None, False,
+               "Ragged list: 2000 tensors, log-uniform sizes (30% below 1e5), N_d=7 virtual ranks"),
     "llama_7b_full": ("llama_7b_full", None, True,
                       "Llama-7B list, all N_d=8 ranks emulated in one HBM (~216 GB), "
                       "one fused launch per 5e8-element bucket"),

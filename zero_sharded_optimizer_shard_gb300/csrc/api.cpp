@@ -88,14 +88,13 @@ zero3_status build_args(const zero3_plan* p, int mode, const RankPtrs& rp, int64
         std::memset(&s, 0, sizeof(s));
         s.lo = la;
         s.hi = lb;
-        bool vec = true;
         if (rp.grads) {
             s.gofs = static_cast<int64_t>(r) * p->S - rp.grads_origin;
-            vec = vec && (s.gofs % 8 == 0);
+            s.gphase = static_cast<int32_t>(s.gofs & 7);  // two's complement: also for gofs < 0
         }
         if (rp.full) {
             s.fofs = static_cast<int64_t>(r) * p->S;
-            vec = vec && (s.fofs % 8 == 0);
+            s.fphase = static_cast<int32_t>(s.fofs & 7);
         } else {
             s.fofs = -1;
         }
@@ -126,7 +125,6 @@ zero3_status build_args(const zero3_plan* p, int mode, const RankPtrs& rp, int64
             if (la % z3::kQwzBlock != 0 || (lb % z3::kQwzBlock != 0 && lb != p->S))
                 return ZERO3_EINVAL;
         }
-        s.vec = vec ? 1 : 0;
         add_span(a, s, rp.warp_blocks);
     }
     return ZERO3_OK;
@@ -161,7 +159,6 @@ zero3_status persistent_launch(const zero3_plan* p, const z3::Scalars& sc,
     s.m = ps->m;
     s.v = ps->v;
     s.out = ps->param;
-    s.vec = 1;
     add_span(a, s);
     return cuda_status(z3::launch_stream(z3::kFused, a, stream));
 }
@@ -214,8 +211,9 @@ zero3_status gather_submodule(const zero3_plan* p, int32_t k, const uint16_t* co
         g.dst_off = dst_off;
         g.len = len;
         g.chunk0 = a.total_chunks;
+        // phase of the source element that lands on an aligned chunk of out
         const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
-        g.vec = ((sa - 2u * static_cast<uintptr_t>(dst_off)) % 16u == 0) ? 1 : 0;
+        g.sphase = static_cast<int32_t>(((sa - 2u * static_cast<uintptr_t>(dst_off)) % 16u) / 2u);
         a.total_chunks += ((dst_off + len) - (dst_off & ~static_cast<int64_t>(7)) + 7) / 8;
         return ZERO3_OK;
     };
@@ -464,7 +462,6 @@ zero3_status zero3_cast_params(const zero3_plan* p, const float* const* master,
         s.fofs = -1;
         s.in = persist->master;
         s.out = persist->param;
-        s.vec = 1;
         add_span(a, s);
         return cuda_status(z3::launch_stream(z3::kCast, a, stream));
     }

@@ -71,8 +71,12 @@ struct Span {
     const void* in;      // shard grad (kAdam) or sparam (kGather, kQuant) or master (kCast)
     int8_t* codes;       // qwZ codes of the shard (kFusedQ, kQuant out; kDequant in)
     float* scales;       // qwZ block scales of the shard
-    int32_t vec;         // 1 when full chunks may use 16-byte vector accesses
-    int32_t pad_;
+    // Element phase (address / 2 mod 8) of the gradient and all-gather
+    // streams at local index 0; states and shards are always 16-byte aligned
+    // at multiples of 8.  Interior chunks load/store the phased streams at
+    // the widest aligned width (16, 8, 4 or 2 bytes).
+    int32_t gphase;
+    int32_t fphase;
 };
 
 struct StreamArgs {
@@ -95,7 +99,7 @@ struct GatherSeg {
     int64_t dst_off;       // offset of the piece in out
     int64_t len;
     int64_t chunk0;
-    int32_t vec;
+    int32_t sphase;        // element phase of the source at an aligned chunk of out
     int32_t pad_;
 };
 struct GatherArgs {

@@ -12,9 +12,10 @@
 // Thread c of the grid takes chunk c, so the 32 lanes of a warp
 // touch 32 adjacent chunks: 512 contiguous bytes of every bf16 stream and
 // 1 KiB of every fp32 stream per warp instruction pair.  Interior chunks of a
-// span whose streams are all 16-byte aligned use 16-byte loads and stores;
-// the edge chunks of a span, and spans whose gradient or all-gather offsets
-// are not multiples of 8 elements, take the element-by-element path.
+// span use 16-byte accesses for the states and shards and the widest aligned
+// width for the gradient and all-gather streams (whose offsets need not be
+// multiples of 8 elements); the edge chunks of a span take the
+// element-by-element path.
 //
 // Arithmetic per element follows the fixed order of the AdamW reading with
 // IEEE round-to-nearest intrinsics (no contraction into FMA):
@@ -76,6 +77,53 @@ __device__ __forceinline__ void stcs_f4(float* p, float4 x) {
     __stcs(reinterpret_cast<float4*>(p), x);
 }
 
+// 8 consecutive bf16 values starting at an address of element phase ph
+// (address / 2 mod 8): one 16-byte load when aligned, else the widest
+// aligned loads (8, 4 or 2 bytes) through the read-only path, so that the
+// bytes neighbouring threads share are served from L1.
+__device__ __forceinline__ uint4 ld8_phase(const uint16_t* p, int ph) {
+    if (ph == 0) return ldcs16(p);
+    if ((ph & 3) == 0) {
+        const uint2 a = __ldg(reinterpret_cast<const uint2*>(p));
+        const uint2 b = __ldg(reinterpret_cast<const uint2*>(p + 4));
+        return make_uint4(a.x, a.y, b.x, b.y);
+    }
+    if ((ph & 1) == 0) {
+        const unsigned int* q = reinterpret_cast<const unsigned int*>(p);
+        return make_uint4(__ldg(q), __ldg(q + 1), __ldg(q + 2), __ldg(q + 3));
+    }
+    const unsigned short* q = reinterpret_cast<const unsigned short*>(p);
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        w[k] = static_cast<uint32_t>(__ldg(q + 2 * k)) |
+               (static_cast<uint32_t>(__ldg(q + 2 * k + 1)) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// 8 consecutive bf16 values stored at an address of element phase ph.
+__device__ __forceinline__ void st8_phase(uint16_t* p, int ph, const uint4& h) {
+    if (ph == 0) {
+        stcs16(p, h);
+    } else if ((ph & 3) == 0) {
+        __stcs(reinterpret_cast<uint2*>(p), make_uint2(h.x, h.y));
+        __stcs(reinterpret_cast<uint2*>(p + 4), make_uint2(h.z, h.w));
+    } else if ((ph & 1) == 0) {
+        unsigned int* q = reinterpret_cast<unsigned int*>(p);
+        __stcs(q, h.x);
+        __stcs(q + 1, h.y);
+        __stcs(q + 2, h.z);
+        __stcs(q + 3, h.w);
+    } else {
+        const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            p[2 * k] = static_cast<uint16_t>(w[k] & 0xffffu);
+            p[2 * k + 1] = static_cast<uint16_t>(w[k] >> 16);
+        }
+    }
+}
+
 __device__ __forceinline__ void unpack8(const uint4& r, float* f) {
     f[0] = bf16_lo(r.x); f[1] = bf16_hi(r.x);
     f[2] = bf16_lo(r.y); f[3] = bf16_hi(r.y);
@@ -88,15 +136,22 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
                       pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
 }
 
-// Reduced gradient of 8 aligned elements, ranks summed in ascending order.
+// Reduced gradient of 8 consecutive elements, ranks summed in ascending
+// order; ph is the element phase of the gradient streams (equal for every
+// rank).  All loads are issued before the first add.
 template <int ND>
-__device__ __forceinline__ void reduce8(const StreamArgs& a, int64_t off, float* g) {
+__device__ __forceinline__ void reduce8(const StreamArgs& a, int64_t off, int ph, float* g) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) g[e] = 0.0f;
     if constexpr (ND > 0) {
         uint4 raw[ND];
+        if (ph == 0) {
 #pragma unroll
-        for (int q = 0; q < ND; ++q) raw[q] = ldcs16(a.grads[q] + off);
+            for (int q = 0; q < ND; ++q) raw[q] = ldcs16(a.grads[q] + off);
+        } else {
+#pragma unroll
+            for (int q = 0; q < ND; ++q) raw[q] = ld8_phase(a.grads[q] + off, ph);
+        }
 #pragma unroll
         for (int q = 0; q < ND; ++q) {
             float f[8];
@@ -111,7 +166,7 @@ __device__ __forceinline__ void reduce8(const StreamArgs& a, int64_t off, float*
             const int n = (nd - q0) < 8 ? (nd - q0) : 8;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-                if (k < n) raw[k] = ldcs16(a.grads[q0 + k] + off);
+                if (k < n) raw[k] = ld8_phase(a.grads[q0 + k] + off, ph);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 if (k < n) {
@@ -140,7 +195,7 @@ __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp
                                              float* hq) {
     float g[8];
     if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ || MODE == kReduce)
-        reduce8<ND>(a, sp.gofs + i0, g);
+        reduce8<ND>(a, sp.gofs + i0, sp.gphase, g);
     if constexpr (MODE == kQuant) {
         unpack8(ldcs16(static_cast<const uint16_t*>(sp.in) + i0), hq);
         return;
@@ -166,7 +221,7 @@ __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp
                 y[e] = __fmul_rn(static_cast<float>(c), sc);
             }
         }
-        stcs16(a.full + sp.fofs + i0, pack8(y));
+        st8_phase(a.full + sp.fofs + i0, sp.fphase, pack8(y));
         return;
     }
 
@@ -182,7 +237,7 @@ __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp
     }
     if constexpr (MODE == kGather) {
         const uint4 x = ldcs16(static_cast<const uint16_t*>(sp.in) + i0);
-        stcs16(a.full + sp.fofs + i0, x);
+        st8_phase(a.full + sp.fofs + i0, sp.fphase, x);
         return;
     }
     if constexpr (MODE == kAdam) {
@@ -229,11 +284,11 @@ __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp
 #pragma unroll
         for (int q = 0; q < (ND > 0 ? ND : ZERO3_MAX_RANKS); ++q) {
             if (ND == 0 && q >= nd) break;
-            stcs16(a.reps[q] + sp.fofs + i0, h);
+            st8_phase(a.reps[q] + sp.fofs + i0, sp.fphase, h);
         }
     } else {
         stcs16(static_cast<uint16_t*>(sp.out) + i0, h);
-        if (sp.fofs >= 0) stcs16(a.full + sp.fofs + i0, h);
+        if (sp.fofs >= 0) st8_phase(a.full + sp.fofs + i0, sp.fphase, h);
     }
 }
 
@@ -376,7 +431,7 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const __grid_constant_
             const Span& sp = a.span[s];
             const int64_t i0 = (sp.lo & ~static_cast<int64_t>(7)) + ((c - sp.chunk0) << 3);
             float hq[8];
-            if (sp.vec && i0 >= sp.lo && i0 + 8 <= sp.hi)
+            if (i0 >= sp.lo && i0 + 8 <= sp.hi)
                 vector_chunk<MODE, ND, GT>(a, sp, i0, hq);
             else
                 scalar_chunk<MODE, ND, GT>(a, sp, i0, hq);
@@ -398,8 +453,8 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
             const GatherSeg& g = a.seg[s];
             const int64_t d0 = (g.dst_off & ~static_cast<int64_t>(7)) + ((c - g.chunk0) << 3);
             const int64_t end = g.dst_off + g.len;
-            if (g.vec && d0 >= g.dst_off && d0 + 8 <= end) {
-                const uint4 x = ldcs16(g.src + (d0 - g.dst_off));
+            if (d0 >= g.dst_off && d0 + 8 <= end) {
+                const uint4 x = ld8_phase(g.src + (d0 - g.dst_off), g.sphase);
                 *reinterpret_cast<uint4*>(a.out + d0) = x;
             } else {
                 for (int e = 0; e < 8; ++e) {
@@ -435,7 +490,11 @@ cudaError_t launch_nd(const StreamArgs& a, cudaStream_t stream) {
     switch (a.nd) {
         case 1: return launch_one<MODE, 1, GT>(a, stream);
         case 2: return launch_one<MODE, 2, GT>(a, stream);
+        case 3: return launch_one<MODE, 3, GT>(a, stream);
         case 4: return launch_one<MODE, 4, GT>(a, stream);
+        case 5: return launch_one<MODE, 5, GT>(a, stream);
+        case 6: return launch_one<MODE, 6, GT>(a, stream);
+        case 7: return launch_one<MODE, 7, GT>(a, stream);
         case 8: return launch_one<MODE, 8, GT>(a, stream);
         default: return launch_one<MODE, 0, GT>(a, stream);
     }

@@ -200,31 +200,6 @@ __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp
         unpack8(ldcs16(static_cast<const uint16_t*>(sp.in) + i0), hq);
         return;
     }
-    if constexpr (MODE == kDequant) {
-        const float sc = sp.scales[i0 / kQwzBlock];
-        float y[8];
-        if constexpr (GT == 4) {
-            // 8 two's-complement nibbles, element i0+e in bits 4e..4e+3
-            const uint32_t w = __ldcs(reinterpret_cast<const unsigned int*>(
-                reinterpret_cast<const uint8_t*>(sp.codes) + i0 / 2));
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int c = static_cast<int>(w << (28 - 4 * e)) >> 28;
-                y[e] = __fmul_rn(static_cast<float>(c), sc);
-            }
-        } else {
-            const uint2 q = __ldcs(reinterpret_cast<const uint2*>(sp.codes + i0));
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint32_t w = e < 4 ? q.x : q.y;
-                const int8_t c = static_cast<int8_t>((w >> (8 * (e & 3))) & 0xffu);
-                y[e] = __fmul_rn(static_cast<float>(c), sc);
-            }
-        }
-        st8_phase(a.full + sp.fofs + i0, sp.fphase, pack8(y));
-        return;
-    }
-
     if constexpr (MODE == kReduce) {
         if constexpr (GT == ZERO3_BF16) {
             stcs16(static_cast<uint16_t*>(sp.out) + i0, pack8(g));
@@ -233,11 +208,6 @@ __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp
             stcs_f4(o, make_float4(g[0], g[1], g[2], g[3]));
             stcs_f4(o + 4, make_float4(g[4], g[5], g[6], g[7]));
         }
-        return;
-    }
-    if constexpr (MODE == kGather) {
-        const uint4 x = ldcs16(static_cast<const uint16_t*>(sp.in) + i0);
-        st8_phase(a.full + sp.fofs + i0, sp.fphase, x);
         return;
     }
     if constexpr (MODE == kAdam) {
@@ -416,6 +386,70 @@ __host__ __device__ constexpr int chunks_per_thread() {
     return (MODE == kDequant || MODE == kGather) ? kCopyChunks : 1;
 }
 
+// The copy-like modes (all-gather copy, dequantizing all-gather): every
+// chunk of the thread is loaded before any is stored.  The compiler cannot
+// hoist a load above a store through another pointer (they may alias), so a
+// load-store loop would keep one load in flight per thread.  Edge chunks of
+// a span take the element path in the first phase.
+template <int MODE, int GT>
+__device__ __forceinline__ void copy_chunks(const StreamArgs& a, int64_t base, int& s) {
+    constexpr int CPT = kCopyChunks;
+    uint4 raw[CPT];      // kGather: 8 bf16; kDequant: the codes (.x, and .y for int8)
+    float scl[CPT];      // kDequant: the block scale
+    uint16_t* dst[CPT];  // first element of the chunk in `full`, or null
+    int ph[CPT];
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+        dst[j] = nullptr;
+        const int64_t c = base + static_cast<int64_t>(j) * blockDim.x;
+        if (c >= a.total_chunks) continue;
+        while (s + 1 < a.n_spans && c >= a.span[s + 1].chunk0) ++s;
+        const Span& sp = a.span[s];
+        const int64_t i0 = (sp.lo & ~static_cast<int64_t>(7)) + ((c - sp.chunk0) << 3);
+        if (i0 >= sp.lo && i0 + 8 <= sp.hi) {
+            if constexpr (MODE == kGather) {
+                raw[j] = ldcs16(static_cast<const uint16_t*>(sp.in) + i0);
+            } else if constexpr (GT == 4) {
+                // 8 two's-complement nibbles, element i0+e in bits 4e..4e+3
+                raw[j].x = __ldcs(reinterpret_cast<const unsigned int*>(
+                    reinterpret_cast<const uint8_t*>(sp.codes) + i0 / 2));
+                scl[j] = sp.scales[i0 / kQwzBlock];
+            } else {
+                const uint2 q = __ldcs(reinterpret_cast<const uint2*>(sp.codes + i0));
+                raw[j].x = q.x;
+                raw[j].y = q.y;
+                scl[j] = sp.scales[i0 / kQwzBlock];
+            }
+            dst[j] = a.full + sp.fofs + i0;
+            ph[j] = sp.fphase;
+        } else {
+            float unused[8];
+            scalar_chunk<MODE, 1, GT>(a, sp, i0, unused);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+        if (!dst[j]) continue;
+        if constexpr (MODE == kGather) {
+            st8_phase(dst[j], ph[j], raw[j]);
+        } else {
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                int c;
+                if constexpr (GT == 4) {
+                    c = static_cast<int>(raw[j].x << (28 - 4 * e)) >> 28;
+                } else {
+                    const uint32_t w = e < 4 ? raw[j].x : raw[j].y;
+                    c = static_cast<int8_t>((w >> (8 * (e & 3))) & 0xffu);
+                }
+                y[e] = __fmul_rn(static_cast<float>(c), scl[j]);
+            }
+            st8_phase(dst[j], ph[j], pack8(y));
+        }
+    }
+}
+
 template <int MODE, int ND, int GT>
 __global__ void __launch_bounds__(kThreads) stream_kernel(const __grid_constant__ StreamArgs a) {
     constexpr int CPT = chunks_per_thread<MODE>();
@@ -423,39 +457,52 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const __grid_constant_
     int s = 0;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * CPT + threadIdx.x;
          base < a.total_chunks; base += stride) {
+        if constexpr (MODE == kGather || MODE == kDequant) {
+            copy_chunks<MODE, GT>(a, base, s);
+        } else {
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-            const int64_t c = base + static_cast<int64_t>(j) * blockDim.x;
-            if (c >= a.total_chunks) break;
-            while (s + 1 < a.n_spans && c >= a.span[s + 1].chunk0) ++s;
-            const Span& sp = a.span[s];
-            const int64_t i0 = (sp.lo & ~static_cast<int64_t>(7)) + ((c - sp.chunk0) << 3);
-            float hq[8];
-            if (i0 >= sp.lo && i0 + 8 <= sp.hi)
-                vector_chunk<MODE, ND, GT>(a, sp, i0, hq);
-            else
-                scalar_chunk<MODE, ND, GT>(a, sp, i0, hq);
-            if constexpr (MODE == kFusedQ || MODE == kQuant) qwz_block<GT == 4 ? 4 : 8>(sp, i0, hq);
+            for (int j = 0; j < CPT; ++j) {
+                const int64_t c = base + static_cast<int64_t>(j) * blockDim.x;
+                if (c >= a.total_chunks) break;
+                while (s + 1 < a.n_spans && c >= a.span[s + 1].chunk0) ++s;
+                const Span& sp = a.span[s];
+                const int64_t i0 = (sp.lo & ~static_cast<int64_t>(7)) + ((c - sp.chunk0) << 3);
+                float hq[8];
+                if (i0 >= sp.lo && i0 + 8 <= sp.hi)
+                    vector_chunk<MODE, ND, GT>(a, sp, i0, hq);
+                else
+                    scalar_chunk<MODE, ND, GT>(a, sp, i0, hq);
+                if constexpr (MODE == kFusedQ || MODE == kQuant)
+                    qwz_block<GT == 4 ? 4 : 8>(sp, i0, hq);
+            }
         }
     }
 }
 
+// A thread's kCopyChunks chunks are loaded before any of them is stored: the
+// compiler cannot move a load above a store to `out` (the pointers may
+// alias), so a load-store-load-store loop keeps one 16-byte load in flight
+// per thread.  Edge chunks of a piece (rare) are copied element by element
+// in the first phase.
 __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherArgs a) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * kCopyChunks;
     int s = 0;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * kCopyChunks + threadIdx.x;
          base < a.total_chunks; base += stride) {
+        uint4 x[kCopyChunks];
+        int64_t dst[kCopyChunks];   // element index of a vector store, or -1
 #pragma unroll
         for (int j = 0; j < kCopyChunks; ++j) {
+            dst[j] = -1;
             const int64_t c = base + static_cast<int64_t>(j) * blockDim.x;
-            if (c >= a.total_chunks) break;
+            if (c >= a.total_chunks) continue;
             while (s + 1 < a.n_segs && c >= a.seg[s + 1].chunk0) ++s;
             const GatherSeg& g = a.seg[s];
             const int64_t d0 = (g.dst_off & ~static_cast<int64_t>(7)) + ((c - g.chunk0) << 3);
             const int64_t end = g.dst_off + g.len;
             if (d0 >= g.dst_off && d0 + 8 <= end) {
-                const uint4 x = ld8_phase(g.src + (d0 - g.dst_off), g.sphase);
-                *reinterpret_cast<uint4*>(a.out + d0) = x;
+                x[j] = ld8_phase(g.src + (d0 - g.dst_off), g.sphase);
+                dst[j] = d0;
             } else {
                 for (int e = 0; e < 8; ++e) {
                     const int64_t d = d0 + e;
@@ -463,6 +510,9 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
                 }
             }
         }
+#pragma unroll
+        for (int j = 0; j < kCopyChunks; ++j)
+            if (dst[j] >= 0) *reinterpret_cast<uint4*>(a.out + dst[j]) = x[j];
     }
 }
 

@@ -174,6 +174,28 @@ def make_workload(args):
     return w
 
 
+def step_config(args, w, world, psi_pad, psi_s, n_flat, sub_numels):
+    """The `config` object of the step benchmark, from the partition's sizes
+    alone, so that both arms (GPU path and CPU oracle) report the same one.
+    Bytes per step: the fused step (2*N_d + 28 per flat element), the
+    persistent group (2*N_d + 26) and two gathers of every submodule (4)."""
+    nd = w.n_ranks
+    total = n_flat * (2 * nd + 28) + psi_s * (2 * nd + 26) + 2 * sum(sub_numels) * 4
+    desc = WORKLOADS[args.workload][3]
+    if args.n_ranks:
+        desc += f" (N_d overridden to {nd})"
+    params = w.psi if WORKLOADS[args.workload][1] is None else n_flat + psi_s
+    return {
+        "workload": desc, "name": args.workload, "n_ranks": nd,
+        "params": params, "psi_pad": psi_pad, "psi_s": psi_s,
+        "bytes_per_step": total,
+        "step": "forward + backward gather of every submodule, fused step, persistent group",
+        "l2": f"inputs larger than L2 ({total / 1e9:.1f} GB touched per step)",
+        "grads": "generated once on the device before timing, reused by every step",
+        "parallelism": f"{world} replica(s) x {nd} emulated ranks",
+    }
+
+
 def cpu_oracle_rate(w, budget_s: float = 15.0):
     """The CPU oracle, as it stands, on a bounded contiguous sample of rank
     0's shard: all N_d ranks' gradients for the sample, the reduce, AdamW and
@@ -216,6 +238,12 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    import oracle as O
+    w = make_workload(args)
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    n_flat = plan.psi_pad if WORKLOADS[args.workload][1] is None else plan.shard_len
+    config = step_config(args, w, args.gpus, plan.psi_pad, plan.psi_s, n_flat,
+                         [plan.submodule_numel(k) for k in range(plan.n_submodules)])
     budget = 4.0
     rates = []
     desc = None
@@ -227,9 +255,12 @@ def run_reference(args):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        # the oracle's time for one whole step of the workload, extrapolated
+        # from the sample's rate
+        "ms_per_step": config["params"] / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOADS[args.workload][3]},
+        "config": config,
         "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
@@ -590,10 +621,8 @@ def run_ours(args):
     from zero_sharded_optimizer_shard_gb300 import workloads as W, zero3
     from zero_sharded_optimizer_shard_gb300.emulation import Emulation
 
-    fac, state_ranks, bucketed, desc = WORKLOADS[args.workload]
+    fac, state_ranks, bucketed, _ = WORKLOADS[args.workload]
     w = make_workload(args)
-    if args.n_ranks:
-        desc += f" (N_d overridden to {w.n_ranks})"
     stream = torch.cuda.Stream()
     e = Emulation(w, device=f"cuda:{local}", state_ranks=state_ranks, bucketed=bucketed,
                   stream=stream)
@@ -679,15 +708,9 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": "f32",
             "data": "synthetic",
-            "config": {
-                "workload": desc, "name": args.workload, "n_ranks": w.n_ranks,
-                "params": n_params, "psi_pad": e.psi_pad, "psi_s": e.psi_s,
-                "bytes_per_step": nbytes["total"],
-                "step": "forward + backward gather of every submodule, fused step, persistent group",
-                "l2": f"inputs larger than L2 ({nbytes['total'] / 1e9:.1f} GB touched per step)",
-                "grads": "generated once on the device before timing, reused by every step",
-                "parallelism": f"{world} replica(s) x {w.n_ranks} emulated ranks",
-            },
+            "config": step_config(args, w, world, e.psi_pad, e.psi_s, nbytes["flat_elems"],
+                                  [e.plan.submodule(k)[1]
+                                   for k in range(e.plan.info.n_submodules)]),
             "step_gbs": step_gbs,
             "step_hbm_frac": step_gbs / peak,
             "fused_step": {"ms_per_launch": fused_launch_ms, "launches_per_step": len(e.chunks),

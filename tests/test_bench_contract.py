@@ -29,7 +29,8 @@ def test_reference_arm_line():
     assert d["unit"] == "params/s" and d["value"] > 0 and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
-    assert d["config"]["workload"]
+    assert d["config"]["workload"] and d["config"]["bytes_per_step"] > 0
+    assert d["ms_per_step"] > 0
 
 
 @pytest.mark.gpu
@@ -44,3 +45,9 @@ def test_our_arm_line():
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] > 0 and {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+    # the reference arm reports the same workload description
+    ref = run_bench("--impl", "reference", "--workload", "gpt2_small", "--steps", "1",
+                    "--warmup", "0")
+    assert ref["config"] == d["config"]
+    assert (ref["metric"], ref["unit"], ref["higher_is_better"]) == \
+        (d["metric"], d["unit"], d["higher_is_better"])

@@ -380,10 +380,16 @@ __device__ __forceinline__ void qwz_block(const Span& sp, int64_t i0, const floa
 // (dequantizing all-gather) at 1.3B.  The fused modes keep one chunk per
 // thread (more registers per chunk; 2 per thread measured slightly slower).
 constexpr int kCopyChunks = 4;
+// The int4 dequantizing all-gather loads only 4 bytes of codes per chunk.
+constexpr int kCopyChunksInt4 = 4;
+// Submodule gather (zero3_fetch_submodule and the prefetch coordinator).
+constexpr int kFetchChunks = 4;
 
-template <int MODE>
+template <int MODE, int GT>
 __host__ __device__ constexpr int chunks_per_thread() {
-    return (MODE == kDequant || MODE == kGather) ? kCopyChunks : 1;
+    return MODE == kGather ? kCopyChunks
+           : MODE == kDequant ? (GT == 4 ? kCopyChunksInt4 : kCopyChunks)
+                              : 1;
 }
 
 // The copy-like modes (all-gather copy, dequantizing all-gather): every
@@ -393,7 +399,7 @@ __host__ __device__ constexpr int chunks_per_thread() {
 // a span take the element path in the first phase.
 template <int MODE, int GT>
 __device__ __forceinline__ void copy_chunks(const StreamArgs& a, int64_t base, int& s) {
-    constexpr int CPT = kCopyChunks;
+    constexpr int CPT = chunks_per_thread<MODE, GT>();
     uint4 raw[CPT];      // kGather: 8 bf16; kDequant: the codes (.x, and .y for int8)
     float scl[CPT];      // kDequant: the block scale
     uint16_t* dst[CPT];  // first element of the chunk in `full`, or null
@@ -452,7 +458,7 @@ __device__ __forceinline__ void copy_chunks(const StreamArgs& a, int64_t base, i
 
 template <int MODE, int ND, int GT>
 __global__ void __launch_bounds__(kThreads) stream_kernel(const __grid_constant__ StreamArgs a) {
-    constexpr int CPT = chunks_per_thread<MODE>();
+    constexpr int CPT = chunks_per_thread<MODE, GT>();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * CPT;
     int s = 0;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * CPT + threadIdx.x;
@@ -479,20 +485,20 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const __grid_constant_
     }
 }
 
-// A thread's kCopyChunks chunks are loaded before any of them is stored: the
+// A thread's kFetchChunks chunks are loaded before any of them is stored: the
 // compiler cannot move a load above a store to `out` (the pointers may
 // alias), so a load-store-load-store loop keeps one 16-byte load in flight
 // per thread.  Edge chunks of a piece (rare) are copied element by element
 // in the first phase.
 __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherArgs a) {
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * kCopyChunks;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * kFetchChunks;
     int s = 0;
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * kCopyChunks + threadIdx.x;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * kFetchChunks + threadIdx.x;
          base < a.total_chunks; base += stride) {
-        uint4 x[kCopyChunks];
-        int64_t dst[kCopyChunks];   // element index of a vector store, or -1
+        uint4 x[kFetchChunks];
+        int64_t dst[kFetchChunks];   // element index of a vector store, or -1
 #pragma unroll
-        for (int j = 0; j < kCopyChunks; ++j) {
+        for (int j = 0; j < kFetchChunks; ++j) {
             dst[j] = -1;
             const int64_t c = base + static_cast<int64_t>(j) * blockDim.x;
             if (c >= a.total_chunks) continue;
@@ -511,7 +517,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
             }
         }
 #pragma unroll
-        for (int j = 0; j < kCopyChunks; ++j)
+        for (int j = 0; j < kFetchChunks; ++j)
             if (dst[j] >= 0) *reinterpret_cast<uint4*>(a.out + dst[j]) = x[j];
     }
 }
@@ -530,7 +536,7 @@ int grid_for(int64_t total_chunks, int chunks_per_thread = 1) {
 
 template <int MODE, int ND, int GT>
 cudaError_t launch_one(const StreamArgs& a, cudaStream_t stream) {
-    const int grid = grid_for(a.total_chunks, chunks_per_thread<MODE>());
+    const int grid = grid_for(a.total_chunks, chunks_per_thread<MODE, GT>());
     if (grid > 0) stream_kernel<MODE, ND, GT><<<grid, kThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
@@ -580,7 +586,7 @@ cudaError_t launch_stream(int mode, const StreamArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream) {
     if (a.total_chunks <= 0) return cudaSuccess;
-    const int grid = grid_for(a.total_chunks, kCopyChunks);
+    const int grid = grid_for(a.total_chunks, kFetchChunks);
     gather_kernel<<<grid, kThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }

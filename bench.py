@@ -633,16 +633,20 @@ def run_ours(args):
     nbytes = e.step_bytes()
     n_params = w.psi if state_ranks is None else nbytes["flat_elems"] + e.psi_s
 
-    def full_step(t, ev_a=None, ev_b=None):
+    def full_step(t, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
         e.forward_backward_gathers()
-        if ev_a is not None:
-            ev_a.record(stream)
+        if ev is not None:
+            ev[1].record(stream)
         for (a_, b_), G in zip(e.chunks, e.grads):
             zero3.zero3_step(e.plan, e.hp, t, e.ptrs(G), a_, e.ptrs(e.master), e.ptrs(e.m),
                              e.ptrs(e.v), e.ptrs(e.sparam), e.full.data_ptr(), None, a_, b_, e.sid)
-        if ev_b is not None:
-            ev_b.record(stream)
+        if ev is not None:
+            ev[2].record(stream)
         zero3.zero3_persistent_step(e.plan, e.hp, t, e.persist, e.sid)
+        if ev is not None:
+            ev[3].record(stream)
 
     t = 0
     for _ in range(args.warmup):
@@ -653,8 +657,7 @@ def run_ours(args):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.5)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
@@ -664,7 +667,7 @@ def run_ours(args):
     start.record(stream)
     for k in range(args.steps):
         t += 1
-        full_step(t, *evs[k])
+        full_step(t, evs[k])
     end.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -672,7 +675,9 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     ms = start.elapsed_time(end)
-    fused_ms = [a.elapsed_time(b) for a, b in evs]
+    gather_ms = [x[0].elapsed_time(x[1]) for x in evs]
+    fused_ms = [x[1].elapsed_time(x[2]) for x in evs]
+    persist_ms = [x[2].elapsed_time(x[3]) for x in evs]
     clk = clocks.stop(tw0, tw1)
     if world > 1:
         ms = reduce_max(ms, f"cuda:{local}")
@@ -718,6 +723,20 @@ def run_ours(args):
                            "bytes_per_elem": 2 * w.n_ranks + 28,
                            "params_per_s": nbytes["flat_elems"] / max(len(e.chunks), 1)
                            / (fused_launch_ms / 1e3)},
+            # every row of the step, timed by events on the launching stream
+            "rows": {
+                "a1_a3_fused": {"ms_per_step": statistics.mean(fused_ms),
+                                "launches": len(e.chunks), "bytes": nbytes["fused"],
+                                "gbs": nbytes["fused"] / statistics.mean(fused_ms) / 1e6},
+                "a4_persistent": {"ms_per_step": statistics.mean(persist_ms), "launches": 1,
+                                  "bytes": nbytes["persistent"],
+                                  "gbs": nbytes["persistent"] / statistics.mean(persist_ms) / 1e6},
+                "a5_gathers": {"ms_per_step": statistics.mean(gather_ms),
+                               "launches": launches_per_step(e) - len(e.chunks)
+                               - (1 if e.psi_s > 0 else 0),
+                               "bytes": nbytes["gathers"],
+                               "gbs": nbytes["gathers"] / statistics.mean(gather_ms) / 1e6},
+            },
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": profile_traffic(kernels_sha())

@@ -38,6 +38,21 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Programmatic dependent launch.  Every kernel of this file is launched with
+// programmatic stream serialization, so it may be scheduled while the
+// previous kernel of the stream drains.  Each thread therefore waits for the
+// previous grids to complete (and their writes to become visible) before its
+// first memory access, which keeps plain stream order for the data; what
+// overlaps is the launch and block dispatch of this grid with the previous
+// grid's tail.  Without a programmatic predecessor the wait returns at once.
+__device__ __forceinline__ void wait_prior_grids() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next programmatic launch of the stream be scheduled.
+__device__ __forceinline__ void allow_next_grid() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 __device__ __forceinline__ float bf16_f32(uint16_t h) {
@@ -458,6 +473,8 @@ __device__ __forceinline__ void copy_chunks(const StreamArgs& a, int64_t base, i
 
 template <int MODE, int ND, int GT>
 __global__ void __launch_bounds__(kThreads) stream_kernel(const __grid_constant__ StreamArgs a) {
+    wait_prior_grids();
+    allow_next_grid();
     constexpr int CPT = chunks_per_thread<MODE, GT>();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * CPT;
     int s = 0;
@@ -491,6 +508,8 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const __grid_constant_
 // per thread.  Edge chunks of a piece (rare) are copied element by element
 // in the first phase.
 __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherArgs a) {
+    wait_prior_grids();
+    allow_next_grid();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * kFetchChunks;
     int s = 0;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * kFetchChunks + threadIdx.x;
@@ -534,11 +553,29 @@ int grid_for(int64_t total_chunks, int chunks_per_thread = 1) {
     return static_cast<int>(need < cap ? need : cap);
 }
 
+// Launch with programmatic stream serialization (see wait_prior_grids).
+template <typename Args>
+cudaError_t launch_programmatic(void (*kernel)(Args), int grid, const Args& a,
+                                cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 template <int MODE, int ND, int GT>
 cudaError_t launch_one(const StreamArgs& a, cudaStream_t stream) {
     const int grid = grid_for(a.total_chunks, chunks_per_thread<MODE, GT>());
-    if (grid > 0) stream_kernel<MODE, ND, GT><<<grid, kThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    if (grid <= 0) return cudaSuccess;
+    const cudaError_t e = launch_programmatic(stream_kernel<MODE, ND, GT>, grid, a, stream);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int MODE, int GT>
@@ -587,8 +624,8 @@ cudaError_t launch_stream(int mode, const StreamArgs& a, cudaStream_t stream) {
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream) {
     if (a.total_chunks <= 0) return cudaSuccess;
     const int grid = grid_for(a.total_chunks, kFetchChunks);
-    gather_kernel<<<grid, kThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    const cudaError_t e = launch_programmatic(gather_kernel, grid, a, stream);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace z3

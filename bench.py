@@ -312,6 +312,8 @@ def setup_single(args, stream=None, **emu_kw):
     torch.cuda.set_device(0)
     fac, state_ranks, bucketed, desc = WORKLOADS[args.workload]
     w = make_workload(args)
+    if args.n_ranks:
+        desc += f" (N_d overridden to {w.n_ranks})"
     stream = stream or torch.cuda.Stream()
     kw = dict(state_ranks=state_ranks, bucketed=bucketed)
     kw.update(emu_kw)
@@ -458,7 +460,7 @@ def run_coordinator(args):
         "metric": "ZeRO-3 forward/backward step with submodule gathers, prefetch on vs off",
         "value": results["prefetch"]["ms_per_step"], "unit": "ms/step", "higher_is_better": False,
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
-        "config": {"workload": WORKLOADS[args.workload][3], "tokens": args.tokens,
+        "config": {"workload": desc, "tokens": args.tokens,
                    "compute": f"bf16 GEMM [{args.tokens} x {width}] x [{width} x numel/{width}] "
                               "per submodule (2 in backward)",
                    "arena_elems": arena_elems, "prefetch_bucket_size": w.bucket},
@@ -597,7 +599,7 @@ def run_unfused(args):
         out[k] = {"ms": ms, "bytes_per_elem": bpe, "gbs": gbs, "frac": gbs / peak}
     unf = sum(out[k]["ms"] for k in ("reduce_scatter", "adamw", "allgather"))
     print(json.dumps({"metric": "unfused vs fused ZeRO-3 step (ablation)", "unit": "ms",
-                      "config": {"workload": WORKLOADS[args.workload][3], "elements": n},
+                      "config": {"workload": desc, "elements": n},
                       "kernels": out, "unfused_ms": unf, "fused_ms": out["fused"]["ms"],
                       "fusion_speedup": unf / out["fused"]["ms"]}))
     return 0

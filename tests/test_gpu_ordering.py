@@ -119,3 +119,40 @@ def test_step_chain_with_torch_kernels_between(dev):
         assert np.array_equal(m0.cpu().numpy().view(np.uint32), st.master[0].view(np.uint32)), t
         assert np.array_equal(u16(f), full), t
         assert np.array_equal(pm.cpu().numpy().view(np.uint32), ps.master.view(np.uint32)), t
+
+
+def test_fused_step_replays_from_a_cuda_graph(dev):
+    """The fused step (flat range + persistent group) captured once in a CUDA
+    graph and replayed three times equals three oracle steps with the same
+    step count and gradients: the launches are capturable, and the
+    programmatic ordering holds between replays."""
+    from tests._oracle_runs import host_grads, host_master, host_pgrads
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    w = W.mini_gpt(4)
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    e, s = emu(w)
+    with torch.cuda.stream(s):
+        e.fill_grads(1)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        e.step(1)
+        zero3.zero3_allgather(e.plan, e.ptrs(e.sparam), e.full.data_ptr(), 0, e.psi_pad, e.sid)
+    torch.cuda.synchronize()
+    snaps = []
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g.replay()
+            snaps.append((e.master[1].clone(), e.v[1].clone(), e.full.clone(), e.pparam.clone()))
+    torch.cuda.synchronize()
+    mf, mp = host_master(w, plan)
+    st, full, ps = O.init_state(plan, mf, mp)
+    G, PG = host_grads(w, plan, 1), host_pgrads(w, plan, 1)
+    for k in range(3):
+        O.sharded_step(plan, w.hparams, 1, G, st, full)
+        O.persistent_step(plan, w.hparams, 1, PG, ps)
+        m1, v1, f, pp = snaps[k]
+        assert np.array_equal(m1.cpu().numpy().view(np.uint32), st.master[1].view(np.uint32)), k
+        assert np.array_equal(v1.cpu().numpy().view(np.uint32), st.v[1].view(np.uint32)), k
+        assert np.array_equal(u16(f), O.allgather(plan, st.sparam)), k
+        assert np.array_equal(u16(pp), ps.param), k

@@ -116,6 +116,35 @@ __device__ __forceinline__ uint4 ld8_phase(const uint16_t* p, int ph) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// The 8 bf16 values at elements ph..ph+7 (1 <= ph <= 7) of the 16-element
+// window formed by two consecutive aligned 16-byte blocks b0, b1 (window
+// words w0..w7).  Branch-free, so the compiler keeps every rank's loads
+// ahead of the first realignment: result word m is the funnel shift of
+// words k+m and k+m+1 (k = ph / 2) right by 16 * (ph & 1) bits, the words
+// picked by two rounds of selects (by 2 words, then by 1).
+__device__ __forceinline__ uint4 realign8(const uint4& b0, const uint4& b1, int ph) {
+    const bool by2 = (ph & 4) != 0, by1 = (ph & 2) != 0;
+    const uint32_t sh = static_cast<uint32_t>(ph & 1) * 16u;
+    const uint32_t t0 = by2 ? b0.z : b0.x, t1 = by2 ? b0.w : b0.y, t2 = by2 ? b1.x : b0.z;
+    const uint32_t t3 = by2 ? b1.y : b0.w, t4 = by2 ? b1.z : b1.x, t5 = by2 ? b1.w : b1.y;
+    const uint32_t v0 = by1 ? t1 : t0, v1 = by1 ? t2 : t1, v2 = by1 ? t3 : t2;
+    const uint32_t v3 = by1 ? t4 : t3, v4 = by1 ? t5 : t4;
+    return make_uint4(__funnelshift_r(v0, v1, sh), __funnelshift_r(v1, v2, sh),
+                      __funnelshift_r(v2, v3, sh), __funnelshift_r(v3, v4, sh));
+}
+
+// 8 consecutive bf16 values at p, element phase ph != 0, read as the two
+// aligned 16-byte blocks around them (through the read-only path, so the
+// block a neighbouring thread also reads is served from L1).  The caller
+// guarantees that both blocks lie inside the valid range: the 8 elements
+// before p and the 16 from p on.
+__device__ __forceinline__ uint4 ld8_window(const uint16_t* p, int ph) {
+    const uint16_t* a = p - ph;
+    const uint4 b0 = __ldg(reinterpret_cast<const uint4*>(a));
+    const uint4 b1 = __ldg(reinterpret_cast<const uint4*>(a + 8));
+    return realign8(b0, b1, ph);
+}
+
 // 8 consecutive bf16 values stored at an address of element phase ph.
 __device__ __forceinline__ void st8_phase(uint16_t* p, int ph, const uint4& h) {
     if (ph == 0) {
@@ -153,9 +182,12 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 
 // Reduced gradient of 8 consecutive elements, ranks summed in ascending
 // order; ph is the element phase of the gradient streams (equal for every
-// rank).  All loads are issued before the first add.
+// rank).  `window`: the chunk's neighbours on both sides lie in the span, so
+// a phased chunk may be read as the two aligned 16-byte blocks around it.
+// All loads are issued before the first add.
 template <int ND>
-__device__ __forceinline__ void reduce8(const StreamArgs& a, int64_t off, int ph, float* g) {
+__device__ __forceinline__ void reduce8(const StreamArgs& a, int64_t off, int ph, bool window,
+                                        float* g) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) g[e] = 0.0f;
     if constexpr (ND > 0) {
@@ -163,6 +195,9 @@ __device__ __forceinline__ void reduce8(const StreamArgs& a, int64_t off, int ph
         if (ph == 0) {
 #pragma unroll
             for (int q = 0; q < ND; ++q) raw[q] = ldcs16(a.grads[q] + off);
+        } else if (window) {
+#pragma unroll
+            for (int q = 0; q < ND; ++q) raw[q] = ld8_window(a.grads[q] + off, ph);
         } else {
 #pragma unroll
             for (int q = 0; q < ND; ++q) raw[q] = ld8_phase(a.grads[q] + off, ph);
@@ -209,8 +244,11 @@ template <int MODE, int ND, int GT>
 __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp, int64_t i0,
                                              float* hq) {
     float g[8];
-    if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ || MODE == kReduce)
-        reduce8<ND>(a, sp.gofs + i0, sp.gphase, g);
+    if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ || MODE == kReduce) {
+        // blocks of a phased chunk: local [i0 - ph, i0 - ph + 16) within [i0 - 8, i0 + 16)
+        const bool window = i0 - 8 >= sp.lo && i0 + 16 <= sp.hi;
+        reduce8<ND>(a, sp.gofs + i0, sp.gphase, window, g);
+    }
     if constexpr (MODE == kQuant) {
         unpack8(ldcs16(static_cast<const uint16_t*>(sp.in) + i0), hq);
         return;
@@ -507,6 +545,10 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const __grid_constant_
 // alias), so a load-store-load-store loop keeps one 16-byte load in flight
 // per thread.  Edge chunks of a piece (rare) are copied element by element
 // in the first phase.
+// PHASED: some piece's source is not 16-byte aligned relative to `out`.  The
+// aligned instantiation keeps fewer registers (one block per chunk) and so
+// more blocks per SM.
+template <bool PHASED>
 __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherArgs a) {
     wait_prior_grids();
     allow_next_grid();
@@ -514,11 +556,17 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
     int s = 0;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * kFetchChunks + threadIdx.x;
          base < a.total_chunks; base += stride) {
-        uint4 x[kFetchChunks];
+        // Phase 1 only issues loads: an aligned source chunk as one 16-byte
+        // block, a phased one as the two aligned blocks around it when both
+        // lie in the piece ([d0 - 8, d0 + 16)).  Realignment waits for the
+        // data, so it happens in phase 2 with the stores.
+        uint4 b0[kFetchChunks], b1[kFetchChunks];
+        int ph[kFetchChunks];   // nonzero: b0, b1 are the blocks around a phased chunk
         int64_t dst[kFetchChunks];   // element index of a vector store, or -1
 #pragma unroll
         for (int j = 0; j < kFetchChunks; ++j) {
             dst[j] = -1;
+            ph[j] = 0;
             const int64_t c = base + static_cast<int64_t>(j) * blockDim.x;
             if (c >= a.total_chunks) continue;
             while (s + 1 < a.n_segs && c >= a.seg[s + 1].chunk0) ++s;
@@ -526,7 +574,17 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
             const int64_t d0 = (g.dst_off & ~static_cast<int64_t>(7)) + ((c - g.chunk0) << 3);
             const int64_t end = g.dst_off + g.len;
             if (d0 >= g.dst_off && d0 + 8 <= end) {
-                x[j] = ld8_phase(g.src + (d0 - g.dst_off), g.sphase);
+                const uint16_t* src = g.src + (d0 - g.dst_off);
+                if (!PHASED || g.sphase == 0) {
+                    b0[j] = ldcs16(src);
+                } else if (d0 - 8 >= g.dst_off && d0 + 16 <= end) {
+                    const uint16_t* al = src - g.sphase;
+                    b0[j] = __ldg(reinterpret_cast<const uint4*>(al));
+                    b1[j] = __ldg(reinterpret_cast<const uint4*>(al + 8));
+                    ph[j] = g.sphase;
+                } else {
+                    b0[j] = ld8_phase(src, g.sphase);
+                }
                 dst[j] = d0;
             } else {
                 for (int e = 0; e < 8; ++e) {
@@ -536,8 +594,11 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
             }
         }
 #pragma unroll
-        for (int j = 0; j < kFetchChunks; ++j)
-            if (dst[j] >= 0) *reinterpret_cast<uint4*>(a.out + dst[j]) = x[j];
+        for (int j = 0; j < kFetchChunks; ++j) {
+            if (dst[j] < 0) continue;
+            const uint4 x = (PHASED && ph[j]) ? realign8(b0[j], b1[j], ph[j]) : b0[j];
+            *reinterpret_cast<uint4*>(a.out + dst[j]) = x;
+        }
     }
 }
 
@@ -624,7 +685,10 @@ cudaError_t launch_stream(int mode, const StreamArgs& a, cudaStream_t stream) {
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream) {
     if (a.total_chunks <= 0) return cudaSuccess;
     const int grid = grid_for(a.total_chunks, kFetchChunks);
-    const cudaError_t e = launch_programmatic(gather_kernel, grid, a, stream);
+    bool phased = false;
+    for (int i = 0; i < a.n_segs; ++i) phased = phased || a.seg[i].sphase != 0;
+    const cudaError_t e = phased ? launch_programmatic(gather_kernel<true>, grid, a, stream)
+                                 : launch_programmatic(gather_kernel<false>, grid, a, stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

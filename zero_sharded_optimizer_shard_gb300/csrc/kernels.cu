@@ -168,6 +168,38 @@ __device__ __forceinline__ void st8_phase(uint16_t* p, int ph, const uint4& h) {
     }
 }
 
+// Warp-cooperative store of a phased stream (1 <= ph <= 7).  All 32 lanes of
+// the warp hold consecutive chunks of one span, so lane i's 8 values go to
+// p + 8 i.  The aligned 16-byte block starting at lane i's element 8 - ph
+// holds lane i's last ph values and lane i+1's first 8 - ph: lanes 0..30
+// store that block (warp_block builds it, the neighbour's values coming by
+// shuffle), lane 31 stores its last ph values and lane 0 its first 8 - ph
+// values element by element.  Every element of the warp's range is written
+// exactly once and nothing outside it.  Every lane of the warp must call
+// warp_block.
+__device__ __forceinline__ uint4 warp_block(int ph, const uint4& h) {
+    uint4 n;
+    n.x = __shfl_down_sync(0xffffffffu, h.x, 1);
+    n.y = __shfl_down_sync(0xffffffffu, h.y, 1);
+    n.z = __shfl_down_sync(0xffffffffu, h.z, 1);
+    n.w = __shfl_down_sync(0xffffffffu, h.w, 1);
+    return realign8(h, n, 8 - ph);
+}
+
+__device__ __forceinline__ void st8_warp(uint16_t* p, int ph, const uint4& h, const uint4& blk) {
+    const int lane = threadIdx.x & 31;
+    const int k = 8 - ph;
+    if (lane < 31) stcs16(p + k, blk);
+    if (lane == 0 || lane == 31) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t w = e < 2 ? h.x : (e < 4 ? h.y : (e < 6 ? h.z : h.w));
+            const uint16_t v = static_cast<uint16_t>((e & 1) ? (w >> 16) : (w & 0xffffu));
+            if (lane == 0 ? e < k : e >= k) p[e] = v;
+        }
+    }
+}
+
 __device__ __forceinline__ void unpack8(const uint4& r, float* f) {
     f[0] = bf16_lo(r.x); f[1] = bf16_hi(r.x);
     f[2] = bf16_lo(r.y); f[3] = bf16_hi(r.y);
@@ -242,7 +274,7 @@ __device__ __forceinline__ float reduce1(const StreamArgs& a, int64_t off) {
 
 template <int MODE, int ND, int GT>
 __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp, int64_t i0,
-                                             float* hq) {
+                                             float* hq, bool warp_store) {
     float g[8];
     if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ || MODE == kReduce) {
         // blocks of a phased chunk: local [i0 - ph, i0 - ph + 16) within [i0 - 8, i0 + 16)
@@ -301,17 +333,25 @@ __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp
     }
     const uint4 h = pack8(p);
     if constexpr (MODE == kFusedQ) unpack8(h, hq);
+    uint4 blk = h;
+    if (warp_store) blk = warp_block(sp.fphase, h);
     if constexpr (MODE == kFusedRep) {
         // all-gather into every rank's full parameter copy
         const int nd = ND > 0 ? ND : a.nd;
 #pragma unroll
         for (int q = 0; q < (ND > 0 ? ND : ZERO3_MAX_RANKS); ++q) {
             if (ND == 0 && q >= nd) break;
-            st8_phase(a.reps[q] + sp.fofs + i0, sp.fphase, h);
+            if (warp_store)
+                st8_warp(a.reps[q] + sp.fofs + i0, sp.fphase, h, blk);
+            else
+                st8_phase(a.reps[q] + sp.fofs + i0, sp.fphase, h);
         }
     } else {
         stcs16(static_cast<uint16_t*>(sp.out) + i0, h);
-        if (sp.fofs >= 0) st8_phase(a.full + sp.fofs + i0, sp.fphase, h);
+        if (warp_store)
+            st8_warp(a.full + sp.fofs + i0, sp.fphase, h, blk);
+        else if (sp.fofs >= 0)
+            st8_phase(a.full + sp.fofs + i0, sp.fphase, h);
     }
 }
 
@@ -509,8 +549,17 @@ __device__ __forceinline__ void copy_chunks(const StreamArgs& a, int64_t base, i
     }
 }
 
+// The fused modes with a compile-time rank count keep 4 blocks of 256
+// threads resident per SM (at most 64 registers a thread): the ZeRO-1/2 step
+// at N_d = 8 otherwise takes 75 and drops to 3 blocks.
+template <int MODE, int ND>
+__host__ __device__ constexpr int min_blocks_per_sm() {
+    return (ND > 0 && (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ)) ? 4 : 1;
+}
+
 template <int MODE, int ND, int GT>
-__global__ void __launch_bounds__(kThreads) stream_kernel(const __grid_constant__ StreamArgs a) {
+__global__ void __launch_bounds__(kThreads, min_blocks_per_sm<MODE, ND>())
+    stream_kernel(const __grid_constant__ StreamArgs a) {
     wait_prior_grids();
     allow_next_grid();
     constexpr int CPT = chunks_per_thread<MODE, GT>();
@@ -529,8 +578,22 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const __grid_constant_
                 const Span& sp = a.span[s];
                 const int64_t i0 = (sp.lo & ~static_cast<int64_t>(7)) + ((c - sp.chunk0) << 3);
                 float hq[8];
-                if (i0 >= sp.lo && i0 + 8 <= sp.hi)
-                    vector_chunk<MODE, ND, GT>(a, sp, i0, hq);
+                const bool vec = i0 >= sp.lo && i0 + 8 <= sp.hi;
+                // A phased all-gather stream is stored by the whole warp at
+                // once when its 32 lanes hold vector chunks of one span (a
+                // warp-uniform decision: every active lane takes part in it,
+                // and a partial or diverged warp keeps the per-lane stores).
+                bool warp_store = false;
+                if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ) {
+                    const unsigned active = __activemask();
+                    if (active == 0xffffffffu) {
+                        const int s0 = __shfl_sync(0xffffffffu, s, 0);
+                        warp_store = __all_sync(0xffffffffu, vec && s == s0 && sp.fofs >= 0 &&
+                                                                 sp.fphase != 0);
+                    }
+                }
+                if (vec)
+                    vector_chunk<MODE, ND, GT>(a, sp, i0, hq, warp_store);
                 else
                     scalar_chunk<MODE, ND, GT>(a, sp, i0, hq);
                 if constexpr (MODE == kFusedQ || MODE == kQuant)

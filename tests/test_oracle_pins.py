@@ -415,6 +415,12 @@ def test_ragged_list_recipe():
     assert runs.min() >= 1 and runs.max() <= 8
 
 
+def test_ragged_list_one_rank_terminates():
+    # every size is divisible by one rank: nothing is redrawn
+    w = W.ragged_small(1)
+    assert len(w.numels) == 300 and w.n_ranks == 1
+
+
 def test_state_machine():
     sm = O.SubmoduleStates(2)
     assert sm.fetch(0) is True and sm.status[0] == O.INFLIGHT

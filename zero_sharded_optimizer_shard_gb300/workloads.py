@@ -148,7 +148,8 @@ def ragged(n_tensors: int = 2000, n_ranks: int = 7, seed: int = 3,
     """Ragged-shape stress list.
 
     Sizes are a p_small / (1 - p_small) mixture of log-uniform [1, small_hi)
-    and log-uniform [big_lo, big_hi], redrawn while divisible by n_ranks.
+    and log-uniform [big_lo, big_hi], redrawn while divisible by n_ranks
+    (for n_ranks > 1; at most 64 draws per tensor, the last one kept).
     Submodules are consecutive runs of 1..8 tensors.  All draws come from the
     counter-based generator (see synth.uniform_u64), so the list is a pure
     function of the seed.
@@ -170,7 +171,7 @@ def ragged(n_tensors: int = 2000, n_ranks: int = 7, seed: int = 3,
             size = int(math.floor(math.exp(math.log(lo) + frac * (math.log(hi) - math.log(lo)))))
             top = int(hi) - 1 if pick < p_small else int(hi)
             size = min(max(size, int(lo)), top)
-            if size % n_ranks != 0:
+            if n_ranks <= 1 or size % n_ranks != 0 or draw == 64:
                 break
         draw = 0
         numels.append(size)

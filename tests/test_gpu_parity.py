@@ -395,3 +395,64 @@ def test_zero_size_tensors(dev):
         n = plan.submodule_numel(k)
         assert np.array_equal(u16(e.out)[:n], O.fetch_submodule(plan, k, st.sparam, ps.param))
         e.release(k)
+
+
+# ---------------------------------------------------------------- every phase
+def all_phase_workload():
+    """Two partitioned tensors and two persistent ones; the shard length is
+    odd at N_d = 8, so rank r's shard starts at element phase (r * S) mod 8
+    and the eight ranks take every phase 0..7 once (gradient and all-gather
+    streams alike)."""
+    return W.Workload("all_phases_nd8", [100_003, 160_005, 17, 99_999], [0, 1, 1, 2],
+                      n_ranks=8, steps=3, seed=21)
+
+
+def test_every_phase_fused_bucketed_and_fetch(dev):
+    """Vector chunks read phased gradients as two aligned blocks, full warps
+    store the phased all-gather cooperatively, span edges take the narrow
+    paths: all bit-exact at every phase.  An odd bucket size shifts the
+    gradient phases against the all-gather phases."""
+    w = all_phase_workload()
+    plan, st, full, ps = oracle_run(w, 3)
+    assert plan.shard_len % 2 == 1
+    assert sorted((r * plan.shard_len) % 8 for r in range(8)) == list(range(8))
+    e = run_device(w, 3)
+    compare_all(e, plan, st, full, ps)
+    for k in range(plan.n_submodules):
+        e.fetch(k)
+        torch.cuda.synchronize()
+        n = plan.submodule_numel(k)
+        assert np.array_equal(u16(e.out)[:n], O.fetch_submodule(plan, k, st.sparam, ps.param)), k
+        e.release(k)
+    wb = all_phase_workload()
+    wb.bucket = 7_919
+    eb = run_device(wb, 3, bucketed=True)
+    assert len(eb.chunks) > 8
+    compare_all(eb, plan, st, full, ps)
+
+
+def test_every_phase_stage12(dev):
+    """The ZeRO-1/2 step writes all N_d full copies through the shared
+    cooperative block at every phase."""
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    from tests._oracle_runs import host_master
+    w = all_phase_workload()
+    w.threshold = 0
+    nd = w.n_ranks
+    plan = O.partition(w.numels, w.submodule_of, nd, 0, w.bucket)
+    assert plan.psi_s == 0 and plan.shard_len % 2 == 1
+    e = make_emu(w)
+    params = [e.full.clone() for _ in range(nd)]
+    mf, mp = host_master(w, plan)
+    st, full, _ = O.init_state(plan, mf, mp)
+    ref = [full.copy() for _ in range(nd)]
+    for t in range(1, 4):
+        e.fill_grads(t)
+        zero3.zero3_step_stage12(e.plan, e.hp, t, e.ptrs(e.grads[0]), 0, e.ptrs(e.master),
+                                 e.ptrs(e.m), e.ptrs(e.v), [x.data_ptr() for x in params], 0,
+                                 e.psi_pad, e.sid)
+        O.replicated_step(plan, w.hparams, t, host_grads(w, plan, t), st, ref)
+    torch.cuda.synchronize()
+    for q in range(nd):
+        assert np.array_equal(u16(params[q]), ref[q]), q
+        assert np.array_equal(bits(f32(e.master[q])), bits(st.master[q])), q

@@ -12,10 +12,14 @@
 // Thread c of the grid takes chunk c, so the 32 lanes of a warp
 // touch 32 adjacent chunks: 512 contiguous bytes of every bf16 stream and
 // 1 KiB of every fp32 stream per warp instruction pair.  Interior chunks of a
-// span use 16-byte accesses for the states and shards and the widest aligned
-// width for the gradient and all-gather streams (whose offsets need not be
-// multiples of 8 elements); the edge chunks of a span take the
-// element-by-element path.
+// span use 16-byte accesses for the states and shards.  The gradient and
+// all-gather streams start at r*S - origin and r*S, which need not be
+// multiples of 8 elements: a chunk at a nonzero element phase reads the two
+// aligned 16-byte blocks around it and realigns them (ld8_window), a whole
+// warp of such chunks stores its all-gather values as aligned blocks passed
+// between neighbouring lanes (st8_warp), chunks next to a span edge use the
+// widest aligned width their phase allows, and the edge chunks themselves
+// take the element-by-element path.
 //
 // Arithmetic per element follows the fixed order of the AdamW reading with
 // IEEE round-to-nearest intrinsics (no contraction into FMA):
@@ -490,16 +494,18 @@ __host__ __device__ constexpr int chunks_per_thread() {
 // hoist a load above a store through another pointer (they may alias), so a
 // load-store loop would keep one load in flight per thread.  Edge chunks of
 // a span take the element path in the first phase.
-template <int MODE, int GT>
+template <int MODE, int GT, bool PHASED>
 __device__ __forceinline__ void copy_chunks(const StreamArgs& a, int64_t base, int& s) {
     constexpr int CPT = chunks_per_thread<MODE, GT>();
     uint4 raw[CPT];      // kGather: 8 bf16; kDequant: the codes (.x, and .y for int8)
     float scl[CPT];      // kDequant: the block scale
     uint16_t* dst[CPT];  // first element of the chunk in `full`, or null
     int ph[CPT];
+    int sidx[CPT];       // span of the chunk
 #pragma unroll
     for (int j = 0; j < CPT; ++j) {
         dst[j] = nullptr;
+        if constexpr (PHASED) sidx[j] = -1;
         const int64_t c = base + static_cast<int64_t>(j) * blockDim.x;
         if (c >= a.total_chunks) continue;
         while (s + 1 < a.n_spans && c >= a.span[s + 1].chunk0) ++s;
@@ -521,6 +527,7 @@ __device__ __forceinline__ void copy_chunks(const StreamArgs& a, int64_t base, i
             }
             dst[j] = a.full + sp.fofs + i0;
             ph[j] = sp.fphase;
+            if constexpr (PHASED) sidx[j] = s;
         } else {
             float unused[8];
             scalar_chunk<MODE, 1, GT>(a, sp, i0, unused);
@@ -528,9 +535,22 @@ __device__ __forceinline__ void copy_chunks(const StreamArgs& a, int64_t base, i
     }
 #pragma unroll
     for (int j = 0; j < CPT; ++j) {
+        // For a fixed j the warp's lanes hold consecutive chunks: a phased
+        // destination is stored by the whole warp when all 32 hold vector
+        // chunks of one span (warp-uniform decision, taken before any lane
+        // leaves the loop body).
+        bool warp_store = false;
+        if constexpr (PHASED) {
+            if (__activemask() == 0xffffffffu) {
+                const int s0 = __shfl_sync(0xffffffffu, sidx[j], 0);
+                warp_store = __all_sync(0xffffffffu,
+                                        dst[j] != nullptr && sidx[j] == s0 && ph[j] != 0);
+            }
+        }
         if (!dst[j]) continue;
+        uint4 x;
         if constexpr (MODE == kGather) {
-            st8_phase(dst[j], ph[j], raw[j]);
+            x = raw[j];
         } else {
             float y[8];
 #pragma unroll
@@ -544,21 +564,35 @@ __device__ __forceinline__ void copy_chunks(const StreamArgs& a, int64_t base, i
                 }
                 y[e] = __fmul_rn(static_cast<float>(c), scl[j]);
             }
-            st8_phase(dst[j], ph[j], pack8(y));
+            x = pack8(y);
         }
+        if (warp_store)
+            st8_warp(dst[j], ph[j], x, warp_block(ph[j], x));
+        else
+            st8_phase(dst[j], ph[j], x);
     }
 }
 
-// The fused modes with a compile-time rank count keep 4 blocks of 256
-// threads resident per SM (at most 64 registers a thread): the ZeRO-1/2 step
-// at N_d = 8 otherwise takes 75 and drops to 3 blocks.
-template <int MODE, int ND>
+// Resident blocks of 256 threads per SM that the register allocation must
+// allow.  The modes that reduce gradients with a compile-time rank count keep
+// 4 (at most 64 registers a thread): the ZeRO-1/2 step at N_d = 8 otherwise
+// takes 75 and the reduce-scatter 80, and both drop to 3 blocks.  The dequantizing all-gather keeps 5 when aligned (at
+// most 48 registers: 6094 against 5656 GB/s with 64) and 4 when phased (3571
+// against 3158 GB/s with 72 at N_d = 7); none of these spills.
+template <int MODE, int ND, bool PHASED>
 __host__ __device__ constexpr int min_blocks_per_sm() {
-    return (ND > 0 && (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ)) ? 4 : 1;
+    return (ND > 0 && (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ ||
+                       MODE == kReduce))                                         ? 4
+           : (MODE == kDequant && !PHASED)                                       ? 5
+           : (MODE == kDequant)                                                  ? 4
+                                                                                 : 1;
 }
 
-template <int MODE, int ND, int GT>
-__global__ void __launch_bounds__(kThreads, min_blocks_per_sm<MODE, ND>())
+// PHASED (copy modes only): some span's all-gather destination is not
+// 16-byte aligned, so the warp-cooperative store path is compiled in; the
+// aligned instantiation keeps fewer registers.
+template <int MODE, int ND, int GT, bool PHASED>
+__global__ void __launch_bounds__(kThreads, min_blocks_per_sm<MODE, ND, PHASED>())
     stream_kernel(const __grid_constant__ StreamArgs a) {
     wait_prior_grids();
     allow_next_grid();
@@ -568,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks_per_sm<MODE, ND>())
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * CPT + threadIdx.x;
          base < a.total_chunks; base += stride) {
         if constexpr (MODE == kGather || MODE == kDequant) {
-            copy_chunks<MODE, GT>(a, base, s);
+            copy_chunks<MODE, GT, PHASED>(a, base, s);
         } else {
 #pragma unroll
             for (int j = 0; j < CPT; ++j) {
@@ -698,7 +732,15 @@ template <int MODE, int ND, int GT>
 cudaError_t launch_one(const StreamArgs& a, cudaStream_t stream) {
     const int grid = grid_for(a.total_chunks, chunks_per_thread<MODE, GT>());
     if (grid <= 0) return cudaSuccess;
-    const cudaError_t e = launch_programmatic(stream_kernel<MODE, ND, GT>, grid, a, stream);
+    cudaError_t e;
+    if constexpr (MODE == kGather || MODE == kDequant) {
+        bool phased = false;
+        for (int i = 0; i < a.n_spans; ++i) phased = phased || a.span[i].fphase != 0;
+        e = phased ? launch_programmatic(stream_kernel<MODE, ND, GT, true>, grid, a, stream)
+                   : launch_programmatic(stream_kernel<MODE, ND, GT, false>, grid, a, stream);
+    } else {
+        e = launch_programmatic(stream_kernel<MODE, ND, GT, false>, grid, a, stream);
+    }
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -474,8 +474,9 @@ __device__ __forceinline__ void qwz_block(const Span& sp, int64_t i0, const floa
 // Chunks per thread.  The copy-like modes move few bytes per chunk (2-3 B
 // per element); a thread then takes 4 chunks, block-interleaved so every
 // warp instruction stays contiguous: measured +9% (gather) and +22%
-// (dequantizing all-gather) at 1.3B.  The fused modes keep one chunk per
-// thread (more registers per chunk; 2 per thread measured slightly slower).
+// (dequantizing all-gather) at 1.3B, and a later sweep of 2 to 16 kept 4.
+// The fused modes keep one chunk per thread (more registers per chunk; 2 per
+// thread measured slightly slower).
 constexpr int kCopyChunks = 4;
 // The int4 dequantizing all-gather loads only 4 bytes of codes per chunk.
 constexpr int kCopyChunksInt4 = 4;
@@ -576,9 +577,10 @@ __device__ __forceinline__ void copy_chunks(const StreamArgs& a, int64_t base, i
 // Resident blocks of 256 threads per SM that the register allocation must
 // allow.  The modes that reduce gradients with a compile-time rank count keep
 // 4 (at most 64 registers a thread): the ZeRO-1/2 step at N_d = 8 otherwise
-// takes 75 and the reduce-scatter 80, and both drop to 3 blocks.  The dequantizing all-gather keeps 5 when aligned (at
-// most 48 registers: 6094 against 5656 GB/s with 64) and 4 when phased (3571
-// against 3158 GB/s with 72 at N_d = 7); none of these spills.
+// takes 75 and the reduce-scatter 80, and both drop to 3 blocks.  The
+// dequantizing all-gather keeps 5 when aligned (at most 48 registers: 6094
+// against 5656 GB/s with 64) and 4 when phased (3571 against 3158 GB/s with
+// 72 at N_d = 7).  None of these spills.
 template <int MODE, int ND, bool PHASED>
 __host__ __device__ constexpr int min_blocks_per_sm() {
     return (ND > 0 && (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ ||

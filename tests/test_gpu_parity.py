@@ -389,6 +389,11 @@ def test_zero_size_tensors(dev):
     plan, st, full, ps = oracle_run(w, 3)
     e = run_device(w, 3)
     compare_all(e, plan, st, full, ps)
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    e.full.zero_()
+    zero3.zero3_allgather(e.plan, e.ptrs(e.sparam), e.full.data_ptr(), 0, e.psi_pad, e.sid)
+    torch.cuda.synchronize()
+    assert np.array_equal(u16(e.full), O.allgather(plan, st.sparam)), "unfused all-gather"
     for k in range(plan.n_submodules):
         e.fetch(k)
         torch.cuda.synchronize()
@@ -418,6 +423,11 @@ def test_every_phase_fused_bucketed_and_fetch(dev):
     assert sorted((r * plan.shard_len) % 8 for r in range(8)) == list(range(8))
     e = run_device(w, 3)
     compare_all(e, plan, st, full, ps)
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    e.full.zero_()
+    zero3.zero3_allgather(e.plan, e.ptrs(e.sparam), e.full.data_ptr(), 0, e.psi_pad, e.sid)
+    torch.cuda.synchronize()
+    assert np.array_equal(u16(e.full), O.allgather(plan, st.sparam)), "unfused all-gather"
     for k in range(plan.n_submodules):
         e.fetch(k)
         torch.cuda.synchronize()

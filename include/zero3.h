@@ -18,6 +18,13 @@
  *    for its state pointers (this is how one device holds only rank 0).
  *  - Compute calls are asynchronous on the given stream.  A kernel fault is
  *    reported as ZERO3_ECUDA by a later call or by zero3_sync.
+ *  - Kernels are launched with programmatic stream serialization: one may be
+ *    scheduled while the previous kernel of its stream is still draining,
+ *    but every thread waits for the previous grids to complete, and their
+ *    writes to be visible, before it touches memory.  Plain stream order
+ *    therefore holds for the data, whatever kernel (this library's or
+ *    another's) comes before or after, and the calls can be captured in a
+ *    CUDA graph.
  *  - A plan is owned by the library: created by zero3_partition, released by
  *    zero3_plan_destroy.  Calls on one plan must not run concurrently from
  *    several host threads.

@@ -58,6 +58,11 @@ struct zero3_coordinator {
     std::vector<int32_t> recording;  // order seen in the current step
     bool trace_ok = false;
     int64_t pos = 0;                 // next trace position
+    // Index of the trace, rebuilt whenever it is set: the positions at which
+    // each submodule is fetched (ascending), and prefix sums of the fetched
+    // elements, so next use and reuse distance cost O(log) and O(1).
+    std::vector<std::vector<int64_t>> uses;
+    std::vector<int64_t> prefix;
 
     int32_t n_sub = 0;
     std::vector<int32_t> status, refs;
@@ -148,19 +153,27 @@ zero3_status drop(zero3_coordinator* c, int32_t k) {
     return ZERO3_OK;
 }
 
+// Rebuilds the index of the trace (may throw std::bad_alloc).
+void index_trace(zero3_coordinator* c) {
+    c->uses.assign(static_cast<size_t>(c->n_sub), {});
+    c->prefix.assign(c->trace.size() + 1, 0);
+    for (size_t j = 0; j < c->trace.size(); ++j) {
+        c->uses[static_cast<size_t>(c->trace[j])].push_back(static_cast<int64_t>(j));
+        c->prefix[j + 1] = c->prefix[j] + numel_of(c, c->trace[j]);
+    }
+}
+
 // Next trace position >= from at which k is fetched again, or -1.
 int64_t next_use(const zero3_coordinator* c, int32_t k, int64_t from) {
     if (!c->trace_ok) return -1;
-    for (int64_t j = from; j < static_cast<int64_t>(c->trace.size()); ++j)
-        if (c->trace[j] == k) return j;
-    return -1;
+    const std::vector<int64_t>& u = c->uses[static_cast<size_t>(k)];
+    const auto it = std::lower_bound(u.begin(), u.end(), from);
+    return it == u.end() ? -1 : *it;
 }
 
 // Gathered elements fetched between trace positions [from, to).
 int64_t distance(const zero3_coordinator* c, int64_t from, int64_t to) {
-    int64_t d = 0;
-    for (int64_t j = from; j < to; ++j) d += numel_of(c, c->trace[j]);
-    return d;
+    return c->prefix[static_cast<size_t>(to)] - c->prefix[static_cast<size_t>(from)];
 }
 
 // Gathers submodule k into a new arena range on the prefetch stream.  With
@@ -294,6 +307,7 @@ zero3_status zero3_coordinator_create(zero3_plan* plan, const int32_t* trace, in
         c->trace.assign(trace, trace + n_trace);
         c->trace_ok = n_trace > 0;
         c->n_sub = n_sub;
+        index_trace(c);
         c->status.assign(n_sub, ZERO3_NOT_AVAILABLE);
         c->refs.assign(n_sub, 0);
         c->off.assign(n_sub, -1);
@@ -402,6 +416,12 @@ zero3_status zero3_coordinator_next_step(zero3_coordinator* c) {
         // adopt the order seen in this step
         c->trace.swap(c->recording);
         c->trace_ok = !c->trace.empty();
+        try {
+            index_trace(c);
+        } catch (const std::bad_alloc&) {
+            c->trace_ok = false;
+            return ZERO3_ENOMEM;
+        }
     }
     c->recording.clear();
     c->pos = 0;

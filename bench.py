@@ -725,19 +725,18 @@ def run_ours(args):
                            "bytes_per_elem": 2 * w.n_ranks + 28,
                            "params_per_s": nbytes["flat_elems"] / max(len(e.chunks), 1)
                            / (fused_launch_ms / 1e3)},
-            # every row of the step, timed by events on the launching stream
+            # every row of the step, timed by events on the launching stream,
+            # against the same measured copy peak as the roofline
             "rows": {
-                "a1_a3_fused": {"ms_per_step": statistics.mean(fused_ms),
-                                "launches": len(e.chunks), "bytes": nbytes["fused"],
-                                "gbs": nbytes["fused"] / statistics.mean(fused_ms) / 1e6},
-                "a4_persistent": {"ms_per_step": statistics.mean(persist_ms), "launches": 1,
-                                  "bytes": nbytes["persistent"],
-                                  "gbs": nbytes["persistent"] / statistics.mean(persist_ms) / 1e6},
-                "a5_gathers": {"ms_per_step": statistics.mean(gather_ms),
-                               "launches": launches_per_step(e) - len(e.chunks)
-                               - (1 if e.psi_s > 0 else 0),
-                               "bytes": nbytes["gathers"],
-                               "gbs": nbytes["gathers"] / statistics.mean(gather_ms) / 1e6},
+                name: dict(ms_per_step=ms_, launches=n_, bytes=b_,
+                           gbs=b_ / ms_ / 1e6 if ms_ > 0 else 0.0,
+                           frac=b_ / ms_ / 1e6 / peak if ms_ > 0 else 0.0)
+                for name, ms_, n_, b_ in (
+                    ("a1_a3_fused", statistics.mean(fused_ms), len(e.chunks), nbytes["fused"]),
+                    ("a4_persistent", statistics.mean(persist_ms), 1, nbytes["persistent"]),
+                    ("a5_gathers", statistics.mean(gather_ms),
+                     launches_per_step(e) - len(e.chunks) - (1 if e.psi_s > 0 else 0),
+                     nbytes["gathers"]))
             },
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,

@@ -45,6 +45,10 @@ def test_our_arm_line():
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] > 0 and {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+    rows = d["rows"]
+    assert set(rows) == {"a1_a3_fused", "a4_persistent", "a5_gathers"}
+    assert all(0 < r["frac"] < 2 and r["launches"] >= 1 for r in rows.values())
+    assert rows["a1_a3_fused"]["frac"] == pytest.approx(r["frac"], rel=1e-6)
     # the reference arm reports the same workload description
     ref = run_bench("--impl", "reference", "--workload", "gpt2_small", "--steps", "1",
                     "--warmup", "0")

@@ -55,3 +55,30 @@ def test_our_arm_line():
     assert ref["config"] == d["config"]
     assert (ref["metric"], ref["unit"], ref["higher_is_better"]) == \
         (d["metric"], d["unit"], d["higher_is_better"])
+
+
+@pytest.mark.parametrize("workload", ["gpt2_small", "ragged", "decoder_1p3b", "llama_7b_full",
+                                      "llama_7b_rank0"])
+def test_arms_describe_the_same_workload(workload, lib):
+    """The GPU arm builds its config from the C library's plan, the reference
+    arm from the oracle's partition: for every workload they must agree (the
+    planner runs on the host, so no GPU is needed)."""
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle as O
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    if workload not in bench.WORKLOADS:
+        pytest.skip(f"no bench workload {workload}")
+    args = argparse.Namespace(workload=workload, n_ranks=None, stage=3)
+    w = bench.make_workload(args)
+    view = bench.WORKLOADS[workload][1] is not None
+    p = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    ref = bench.step_config(args, w, 1, p.psi_pad, p.psi_s, p.shard_len if view else p.psi_pad,
+                            [p.submodule_numel(k) for k in range(p.n_submodules)])
+    plan = zero3.Plan(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    info = plan.info
+    ours = bench.step_config(args, w, 1, info.psi_pad, info.psi_s,
+                             info.shard_len if view else info.psi_pad,
+                             [plan.submodule(k)[1] for k in range(info.n_submodules)])
+    assert ours == ref

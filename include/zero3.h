@@ -432,12 +432,18 @@ void zero3_coordinator_destroy(zero3_coordinator* c);
  *   prime 1099511628211) over the bytes of the int64 values n_ranks,
  *   persistence threshold, tensor count, then every tensor's element count
  * followed by raw little-endian arrays (a shard: fp32 master, m, v of S
- * elements each; the persistent group likewise with psi_s elements).  Loading checks every header field against the plan and the
- * arguments and returns ZERO3_EIO on any mismatch, on a short file or on
- * trailing bytes; nothing is written to device memory before the header has
- * been validated.  Calls are synchronous (they synchronise `stream`); device
- * pointers need no alignment except `full` (16 bytes).  The library stages
- * through a 16 MiB host buffer that it allocates and frees per call. */
+ * elements each; the persistent group likewise with psi_s elements).
+ * Loading checks every header field against the plan and the arguments, and
+ * the file's size against exactly header + arrays, and returns ZERO3_EIO on
+ * any mismatch (a short file and one with trailing bytes included); nothing
+ * is written to device memory before these checks have passed, so a
+ * rejected file leaves the destination buffers as they were.  Saving writes
+ * "<path>.tmp.<pid>", flushes it to disk (fsync) and renames it over `path`
+ * only when every byte has been written; on any error the temporary file is
+ * removed and an existing file at `path` is left unchanged.  Calls are
+ * synchronous (they synchronise `stream`); device pointers need no alignment
+ * except `full` (16 bytes).  The library stages through a 16 MiB host buffer
+ * that it allocates and frees per call. */
 
 /* Writes rank `rank`'s fp32 master, m and v shards (S elements each) and the
  * step count t. */

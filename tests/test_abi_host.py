@@ -353,6 +353,59 @@ def test_merge_shards_matches_oracle(lib, tmp_path):
         zero3.zero3_merge_shards(p, swapped, tmp_path / "p.ckpt", out2)
     with pytest.raises(zero3.Zero3Error):
         zero3.zero3_merge_shards(p, paths[:6] + [tmp_path / "nope"], tmp_path / "p.ckpt", out2)
+    # a shard file one element short, or with one byte too many: EIO, no output
+    _write(paths[3], 1, 3, 7, ref.shard_len, 9, fp, [masters[3], np.zeros(ref.shard_len),
+                                                     np.ones(ref.shard_len)])
+    full3 = paths[3].read_bytes()
+    for bad in (full3[:-4], full3 + b"\0"):
+        paths[3].write_bytes(bad)
+        with pytest.raises(zero3.Zero3Error) as exc:
+            zero3.zero3_merge_shards(p, paths, tmp_path / "p.ckpt", out2)
+        assert exc.value.status == zero3.EIO and not out2.exists()
+
+
+_ATOMIC_CHILD = r'''
+import os, resource, signal, sys
+sys.path.insert(0, {root!r})
+import numpy as np
+from zero_sharded_optimizer_shard_gb300 import workloads as W, zero3
+from tests.test_abi_host import _fnv1a, _write
+w = W.ragged_small(7)
+p = zero3.Plan(w.numels, w.submodule_of, 7, w.threshold, w.bucket)
+info = p.info
+fp = _fnv1a([7, w.threshold, len(w.numels)] + list(w.numels))
+d = {d!r}
+paths = [os.path.join(d, "r%d.ckpt" % r) for r in range(7)]
+for r in range(7):
+    _write(paths[r], 1, r, 7, info.shard_len, 1, fp, [np.full(info.shard_len, r, np.float32)] * 3)
+_write(os.path.join(d, "p.ckpt"), 2, -1, 7, info.psi_s, 1, fp, [np.zeros(info.psi_s)] * 3)
+out = os.path.join(d, "merged.bin")
+# files larger than 64 KiB cannot be written from here on: the merge fails
+# in the middle of writing its output
+signal.signal(signal.SIGXFSZ, signal.SIG_IGN)
+resource.setrlimit(resource.RLIMIT_FSIZE, (1 << 16, 1 << 16))
+try:
+    zero3.zero3_merge_shards(p, paths, os.path.join(d, "p.ckpt"), out)
+except zero3.Zero3Error as e:
+    print("status", e.status)
+'''
+
+
+def test_failed_save_keeps_the_previous_file(lib, tmp_path):
+    """A save that fails in the middle of writing (here: the process may
+    not write files beyond 64 KiB) reports EIO, leaves the file that was at
+    the destination path byte for byte, and leaves no temporary file."""
+    import subprocess
+    import sys
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    out = tmp_path / "merged.bin"
+    out.write_bytes(b"previous checkpoint")
+    code = _ATOMIC_CHILD.format(root=ROOT, d=str(tmp_path))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert f"status {zero3.EIO}" in r.stdout, r.stdout + r.stderr
+    assert out.read_bytes() == b"previous checkpoint"
+    assert sorted(x.name for x in tmp_path.iterdir() if ".tmp." in x.name) == []
 
 
 def test_plan_memory_bytes_matches_oracle(lib):

@@ -12,8 +12,18 @@
 // File = header + raw little-endian arrays.  The header carries a fingerprint
 // of the partition (rank count, threshold, element counts), so a shard can
 // only be loaded into the partitioning that wrote it.
+//
+// Saves never write into the destination path directly: they write a
+// temporary file beside it, flush it to disk and rename it over the path, so
+// a failed or interrupted save (no space, a CUDA error mid-copy, a killed
+// process) leaves the previous file as it was.  Loads check the header and
+// the file's exact size before the first byte reaches device memory.
+#include <sys/stat.h>
+#include <unistd.h>
+
 #include <cstdio>
 #include <cstring>
+#include <string>
 #include <vector>
 
 #include "internal.h"
@@ -76,6 +86,45 @@ struct File {
     }
 };
 
+// Output file written under a temporary name ("<path>.tmp.<pid>") and moved
+// over `path` by commit(): fflush, fsync, fclose, rename.  Destroyed without
+// a successful commit, it removes the temporary file and leaves `path`
+// untouched.
+struct AtomicFile {
+    FILE* f = nullptr;
+    std::string path, tmp;
+    bool done = false;
+    AtomicFile() = default;
+    AtomicFile(const AtomicFile&) = delete;
+    AtomicFile& operator=(const AtomicFile&) = delete;
+    zero3_status open(const char* dst) {
+        try {
+            path = dst;
+            tmp = path + ".tmp." + std::to_string(static_cast<long long>(getpid()));
+        } catch (const std::bad_alloc&) {
+            return ZERO3_ENOMEM;
+        }
+        f = std::fopen(tmp.c_str(), "wb");
+        if (!f) {
+            tmp.clear();
+            return ZERO3_EIO;
+        }
+        return ZERO3_OK;
+    }
+    zero3_status commit() {
+        const bool flushed = std::fflush(f) == 0 && fsync(fileno(f)) == 0;
+        const bool closed = std::fclose(f) == 0;
+        f = nullptr;
+        if (!flushed || !closed || std::rename(tmp.c_str(), path.c_str()) != 0) return ZERO3_EIO;
+        done = true;
+        return ZERO3_OK;
+    }
+    ~AtomicFile() {
+        if (f) std::fclose(f);
+        if (!done && !tmp.empty()) std::remove(tmp.c_str());
+    }
+};
+
 // Copies `bytes` of device memory at src to the file through a host buffer.
 zero3_status write_device(FILE* f, const void* src, int64_t bytes, std::vector<char>& buf,
                           cudaStream_t s) {
@@ -105,11 +154,18 @@ zero3_status read_device(FILE* f, void* dst, int64_t bytes, std::vector<char>& b
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Opens and validates a checkpoint file written for this plan.
+// Opens and validates a checkpoint file written for this plan: every header
+// field, and a total size of exactly the header plus `payload` bytes (a
+// truncated file or one with trailing bytes is rejected here, before any of
+// it is read into device memory).
 zero3_status open_checked(const zero3_plan* p, const char* path, Kind kind, int32_t rank,
-                          int64_t n, File& file, Header& h) {
+                          int64_t n, int64_t payload, File& file, Header& h) {
     file.f = std::fopen(path, "rb");
     if (!file.f) return ZERO3_EIO;
+    struct stat sb;
+    if (fstat(fileno(file.f), &sb) != 0 ||
+        static_cast<int64_t>(sb.st_size) != static_cast<int64_t>(sizeof(Header)) + payload)
+        return ZERO3_EIO;
     if (std::fread(&h, sizeof(h), 1, file.f) != 1) return ZERO3_EIO;
     if (std::memcmp(h.magic, kMagic, 8) != 0 || h.version != kVersion || h.kind != kind ||
         h.rank != rank || h.n_ranks != p->n_ranks || h.n_elems != n ||
@@ -121,9 +177,9 @@ zero3_status open_checked(const zero3_plan* p, const char* path, Kind kind, int3
 zero3_status save_arrays(const zero3_plan* p, const char* path, Kind kind, int32_t rank,
                          int64_t n, int64_t t, const void* const* arrays, int n_arrays,
                          int elem_bytes, cudaStream_t s) {
-    File file;
-    file.f = std::fopen(path, "wb");
-    if (!file.f) return ZERO3_EIO;
+    AtomicFile file;
+    zero3_status st = file.open(path);
+    if (st != ZERO3_OK) return st;
     const Header h = make_header(p, kind, rank, n, t);
     if (std::fwrite(&h, sizeof(h), 1, file.f) != 1) return ZERO3_EIO;
     std::vector<char> buf;
@@ -133,11 +189,10 @@ zero3_status save_arrays(const zero3_plan* p, const char* path, Kind kind, int32
         return ZERO3_ENOMEM;
     }
     for (int k = 0; k < n_arrays; ++k) {
-        zero3_status st = write_device(file.f, arrays[k], n * elem_bytes, buf, s);
+        st = write_device(file.f, arrays[k], n * elem_bytes, buf, s);
         if (st != ZERO3_OK) return st;
     }
-    if (std::fflush(file.f) != 0) return ZERO3_EIO;
-    return ZERO3_OK;
+    return file.commit();
 }
 
 zero3_status load_arrays(const zero3_plan* p, const char* path, Kind kind, int32_t rank,
@@ -145,7 +200,8 @@ zero3_status load_arrays(const zero3_plan* p, const char* path, Kind kind, int32
                          int elem_bytes, cudaStream_t s) {
     File file;
     Header h;
-    zero3_status st = open_checked(p, path, kind, rank, n, file, h);
+    zero3_status st =
+        open_checked(p, path, kind, rank, n, n_arrays * n * elem_bytes, file, h);
     if (st != ZERO3_OK) return st;
     std::vector<char> buf;
     try {
@@ -157,8 +213,6 @@ zero3_status load_arrays(const zero3_plan* p, const char* path, Kind kind, int32
         st = read_device(file.f, arrays[k], n * elem_bytes, buf, s);
         if (st != ZERO3_OK) return st;
     }
-    char extra;
-    if (std::fread(&extra, 1, 1, file.f) != 0) return ZERO3_EIO;  // trailing bytes
     *t = h.t;
     return ZERO3_OK;
 }
@@ -221,9 +275,9 @@ zero3_status zero3_save_16bit_weights(const zero3_plan* p, const uint16_t* full,
     if (!p || !path) return ZERO3_EINVAL;
     if (p->psi_p > 0 && (!full || !aligned16(full))) return ZERO3_EINVAL;
     if (p->psi_s > 0 && !persist_param) return ZERO3_EINVAL;
-    File file;
-    file.f = std::fopen(path, "wb");
-    if (!file.f) return ZERO3_EIO;
+    AtomicFile file;
+    zero3_status st0 = file.open(path);
+    if (st0 != ZERO3_OK) return st0;
     const int64_t total = p->psi_p + p->psi_s;
     const Header h = make_header(p, kWeights16, -1, total, 0);
     if (std::fwrite(&h, sizeof(h), 1, file.f) != 1) return ZERO3_EIO;
@@ -240,8 +294,7 @@ zero3_status zero3_save_16bit_weights(const zero3_plan* p, const uint16_t* full,
         zero3_status st = write_device(file.f, src, p->numel[t] * 2, buf, stream);
         if (st != ZERO3_OK) return st;
     }
-    if (std::fflush(file.f) != 0) return ZERO3_EIO;
-    return ZERO3_OK;
+    return file.commit();
 }
 
 zero3_status zero3_merge_shards(const zero3_plan* p, const char* const* shard_paths,
@@ -255,7 +308,8 @@ zero3_status zero3_merge_shards(const zero3_plan* p, const char* const* shard_pa
     int64_t t = -1;
     for (int r = 0; r < p->n_ranks; ++r) {
         Header h;
-        zero3_status st = open_checked(p, shard_paths[r], kShard, r, p->S, shards[r], h);
+        zero3_status st =
+            open_checked(p, shard_paths[r], kShard, r, p->S, 3 * p->S * 4, shards[r], h);
         if (st != ZERO3_OK) return st;
         if (t >= 0 && h.t != t) return ZERO3_EIO;  // shards of different steps
         t = h.t;
@@ -263,14 +317,15 @@ zero3_status zero3_merge_shards(const zero3_plan* p, const char* const* shard_pa
     File pers;
     if (p->psi_s > 0) {
         Header h;
-        zero3_status st = open_checked(p, persistent_path, kPersist, -1, p->psi_s, pers, h);
+        zero3_status st =
+            open_checked(p, persistent_path, kPersist, -1, p->psi_s, 3 * p->psi_s * 4, pers, h);
         if (st != ZERO3_OK) return st;
         if (t >= 0 && h.t != t) return ZERO3_EIO;
         t = h.t;
     }
-    File out;
-    out.f = std::fopen(out_path, "wb");
-    if (!out.f) return ZERO3_EIO;
+    AtomicFile out;
+    zero3_status st0 = out.open(out_path);
+    if (st0 != ZERO3_OK) return st0;
     const Header h = make_header(p, kWeights32, -1, p->psi_p + p->psi_s, t < 0 ? 0 : t);
     if (std::fwrite(&h, sizeof(h), 1, out.f) != 1) return ZERO3_EIO;
     std::vector<char> buf;
@@ -296,8 +351,7 @@ zero3_status zero3_merge_shards(const zero3_plan* p, const char* const* shard_pa
         }
         if (st != ZERO3_OK) return st;
     }
-    if (std::fflush(out.f) != 0) return ZERO3_EIO;
-    return ZERO3_OK;
+    return out.commit();
 }
 
 }  // extern "C"

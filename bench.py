@@ -1,23 +1,27 @@
 """Benchmark of the ZeRO-3 hot path: one step = a forward and a backward
-gather of every submodule plus the fused reduce-scatter/AdamW/cast/all-gather
-step over every virtual rank and the persistent group.
+gather of every submodule (bucketed, allgather_bucket_size elements per call)
+plus the fused reduce-scatter/AdamW/cast/all-gather step over every virtual
+rank and the persistent group.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decoder_1p3b|gpt2_small|llama_7b_rank0]
+                    [--workload decoder_1p3b|gpt2_small|ragged|llama_7b_rank0|...]
+                    [--second auto|none|<workload>]
 
-Prints one JSON line (rank 0).  N > 1 runs one replica of the workload per
-GPU (the emulated ranks live inside each GPU; there is no inter-GPU step),
-launched by torch.distributed.run; value is the params of all replicas per
-second (weak scaling).  --impl reference times the CPU oracle on a bounded
-sample of the same workload.
+Prints one JSON line (rank 0).  The default run measures the 1.3B decoder
+(the headline `value`) and, in the same line under `configs`, the Llama-7B
+rank-0 view.  N > 1 runs one replica of the workload per GPU (the emulated
+ranks live inside each GPU; there is no inter-GPU step), launched by
+torch.distributed.run; value is the params of all replicas per second (weak
+scaling).  --impl reference times the CPU oracle, as it stands, on the
+host's cores on a scaled copy of the same parameter list.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import math
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -28,7 +32,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fused ZeRO-3 step params/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU"
-PROFILE = os.path.join(ROOT, "profiles", "zero3_step_fused_decoder_1p3b.md")
+PROFILE_JSON = os.path.join(ROOT, "profiles", "zero3_step_fused_decoder_1p3b.json")
+# GB300 HBM3e nominal bandwidth (NVIDIA's product figure): the second
+# denominator of the roofline, beside the measured copy rate.
+NOMINAL_HBM_GBS = 7900.0
 
 WORKLOADS = {
     # name: (factory, state ranks, bucketed, description)
@@ -46,17 +53,25 @@ WORKLOADS = {
                        "Llama-7B list (32L, d=4096, SwiGLU 11008, vocab 32000), rank-0 view at "
                        "N_d=8: rank 0's state resident, gradients per 5e8-element bucket"),
 }
+DEFAULT_SECOND = {"decoder_1p3b": "llama_7b_rank0"}
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decoder_1p3b")
+    ap.add_argument("--second", default="auto",
+                    help="second workload measured in the same run and reported under "
+                         "`configs` (auto: the Llama-7B rank-0 view after the 1.3B headline; "
+                         "none: skip)")
     ap.add_argument("--n-ranks", type=int, default=None,
                     help="override the workload's N_d (small profiling cases)")
+    ap.add_argument("--gather-bucket", type=int, default=None,
+                    help="elements per submodule-gather call (allgather_bucket_size; default "
+                         "the workload's 5e8; 0 = one call per submodule)")
     ap.add_argument("--stage", type=int, choices=[2, 3], default=3,
                     help="3: ZeRO-3 step (default); 2: the ZeRO-1/2 step (full parameters on "
                          "every rank, no submodule gathers)")
@@ -74,7 +89,19 @@ def parse():
                          "as three launches, each timed")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--cpu-budget", type=float, default=8.0,
+                    help="seconds of oracle work per CPU-baseline measurement")
+    return ap.parse_args(argv)
+
+
+def second_workload(args):
+    if args.second == "none" or args.n_ranks:
+        return None
+    if args.second == "auto":
+        return DEFAULT_SECOND.get(args.workload)
+    if args.second not in WORKLOADS:
+        raise SystemExit(f"unknown --second workload {args.second}")
+    return args.second if args.second != args.workload else None
 
 
 def peaks():
@@ -86,21 +113,23 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def profile_traffic(kernels_sha: str):
-    """DRAM bytes per launch of the fused kernel from the committed ncu
-    summary, if it was captured on the current kernel source."""
-    if not os.path.exists(PROFILE):
-        return None
-    txt = open(PROFILE).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(kernels\.cu sha256 ([0-9a-f]+)\)", txt)
-    if not m or m.group(2) != kernels_sha:
-        return None
-    return float(m.group(1))
-
-
 def kernels_sha() -> str:
     p = os.path.join(ROOT, "zero_sharded_optimizer_shard_gb300", "csrc", "kernels.cu")
     return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def profile_traffic(workload: str, sha: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu
+    summary (machine-readable copy), if it was captured on the current
+    kernel source; None otherwise."""
+    if not os.path.exists(PROFILE_JSON):
+        return None
+    with open(PROFILE_JSON) as f:
+        d = json.load(f)
+    if d.get("kernels_cu_sha16") != sha:
+        return None
+    v = d.get("traffic_bytes_per_launch", {}).get(workload)
+    return float(v) if v is not None else None
 
 
 class ClockSampler:
@@ -162,107 +191,243 @@ class ClockSampler:
                 "samples": len(inside), "window": window, "reasons": reasons}
 
 
-def make_workload(args):
+def make_workload(args, name=None):
     from zero_sharded_optimizer_shard_gb300 import workloads as W
-    fac = WORKLOADS[args.workload][0]
+    name = name or args.workload
+    fac = WORKLOADS[name][0]
     w = W.llama_7b(rank0_view=(fac == "llama_7b_rank0")) if fac.startswith("llama_7b") \
         else getattr(W, fac)()
-    if args.n_ranks:
+    if getattr(args, "n_ranks", None) and name == args.workload:
         w.n_ranks = args.n_ranks
-    if args.stage == 2:
+    if getattr(args, "stage", 3) == 2:
         w.threshold = 0  # the persistence threshold is a stage-3 setting
+    gb = getattr(args, "gather_bucket", None)
+    if gb is not None:
+        w.gather_bucket = gb
     return w
 
 
-def step_config(args, w, world, psi_pad, psi_s, n_flat, sub_numels):
+def gather_groups(sub_numels, bucket):
+    """Consecutive submodules grouped into all-gather buckets of at most
+    `bucket` elements (0: one submodule per group)."""
+    groups, cur, size = [], [], 0
+    for k, n in enumerate(sub_numels):
+        if cur and (bucket <= 0 or size + n > bucket):
+            groups.append(cur)
+            cur, size = [], 0
+        cur.append(k)
+        size += n
+    if cur:
+        groups.append(cur)
+    return groups
+
+
+def step_config(args, w, world, psi_pad, psi_s, n_flat, sub_numels, name=None):
     """The `config` object of the step benchmark, from the partition's sizes
     alone, so that both arms (GPU path and CPU oracle) report the same one.
     Bytes per step: the fused step (2*N_d + 28 per flat element), the
     persistent group (2*N_d + 26) and two gathers of every submodule (4)."""
+    name = name or args.workload
     nd = w.n_ranks
     total = n_flat * (2 * nd + 28) + psi_s * (2 * nd + 26) + 2 * sum(sub_numels) * 4
-    desc = WORKLOADS[args.workload][3]
-    if args.n_ranks:
+    desc = WORKLOADS[name][3]
+    if getattr(args, "n_ranks", None) and name == args.workload:
         desc += f" (N_d overridden to {nd})"
-    params = w.psi if WORKLOADS[args.workload][1] is None else n_flat + psi_s
+    params = w.psi if WORKLOADS[name][1] is None else n_flat + psi_s
+    groups = gather_groups(sub_numels, w.gather_bucket)
     return {
-        "workload": desc, "name": args.workload, "n_ranks": nd,
+        "workload": desc, "name": name, "n_ranks": nd,
         "params": params, "psi_pad": psi_pad, "psi_s": psi_s,
         "bytes_per_step": total,
-        "step": "forward + backward gather of every submodule, fused step, persistent group",
+        "step": "forward + backward gather of every submodule, fused step with the persistent "
+                "group in the same launch",
+        "gather_bucket": w.gather_bucket, "gather_calls_per_pass": len(groups),
         "l2": f"inputs larger than L2 ({total / 1e9:.1f} GB touched per step)",
         "grads": "generated once on the device before timing, reused by every step",
         "parallelism": f"{world} replica(s) x {nd} emulated ranks",
     }
 
 
-def cpu_oracle_rate(w, budget_s: float = 15.0):
-    """The CPU oracle, as it stands, on a bounded contiguous sample of rank
-    0's shard: all N_d ranks' gradients for the sample, the reduce, AdamW and
-    bf16 cast.  Returns (params/s, description)."""
-    import numpy as np
+# ---------------------------------------------------------------- CPU oracle
+def scaled_workload(w, target_params: int):
+    """The same parameter list with every tensor scaled by f = target/psi
+    (at least one element; zero-size tensors stay empty), the persistence
+    threshold moved so that exactly the same tensors stay unpartitioned,
+    same N_d, submodules and hyper-parameters.  Returns (workload, f)."""
+    import copy
+    f = min(1.0, target_params / max(w.psi, 1))
+    pers = [n0 > 0 and n0 < w.threshold for n0 in w.numels]
+    numels = [0 if n0 == 0 else max(1, int(round(n0 * f))) for n0 in w.numels]
+    thr = max([n for n, p in zip(numels, pers) if p] + [0]) + 1
+    numels = [n if (p or n0 == 0) else max(n, thr) for n, p, n0 in zip(numels, pers, w.numels)]
+    s = copy.copy(w)
+    s.numels, s.threshold, s.name = numels, thr, w.name + "_scaled"
+    s.bucket = max(1, int(w.bucket * f))
+    return s, f
 
+
+def _oracle_inputs(s, view_rank0: bool):
+    """Seeded inputs of the scaled workload (host generator): masters, every
+    rank's gradient (rank 0's range only for the rank-0 view), persistent
+    group."""
+    import numpy as np
     import oracle as O
     from zero_sharded_optimizer_shard_gb300 import synth, workloads as W
+    plan = O.partition(s.numels, s.submodule_of, s.n_ranks, s.threshold, s.bucket)
+    hi = plan.shard_len if view_rank0 else plan.psi_pad
+    mf = np.zeros(plan.psi_pad, np.float32)
+    mf[:plan.psi_p] = synth.normal_f32(s.seed, W.STREAM_MASTER, 0, 0, np.arange(plan.psi_p),
+                                       s.master_sigma)
+    mp = synth.normal_f32(s.seed, W.STREAM_MASTER_PERSIST, 0, 0, np.arange(plan.psi_s),
+                          s.master_sigma)
+    G = np.zeros((plan.n_ranks, plan.psi_pad), np.uint16)
+    n = min(hi, plan.psi_p)
+    for q in range(plan.n_ranks):
+        G[q, :n] = synth.normal_bf16(s.seed, W.STREAM_GRAD, 1, q, np.arange(n), s.grad_sigma,
+                                     s.outlier_p, s.outlier_sigma)
+    PG = np.stack([synth.normal_bf16(s.seed, W.STREAM_GRAD_PERSIST, 1, q, np.arange(plan.psi_s),
+                                     s.grad_sigma, s.outlier_p, s.outlier_sigma)
+                   for q in range(plan.n_ranks)]) if plan.psi_s else \
+        np.zeros((plan.n_ranks, 0), np.uint16)
+    return dict(mf=mf, mp=mp, G=G, PG=PG, hi=np.int64(hi))
 
-    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
-    rng_n = 1 << 20
-    idx = np.arange(rng_n, dtype=np.int64)
-    grads = [synth.normal_bf16(w.seed, W.STREAM_GRAD, 1, q, idx, w.grad_sigma, w.outlier_p,
-                               w.outlier_sigma) for q in range(plan.n_ranks)]
-    p = synth.normal_f32(w.seed, W.STREAM_MASTER, 0, 0, idx, w.master_sigma)
-    m = np.zeros_like(p)
-    v = np.zeros_like(p)
 
-    def one(t, p, m, v):
-        sc = O.adamw_scalars(w.hparams, t, plan.n_ranks)
-        g = O.reduce_sum(grads, sc["inv_nd"])
-        p, m, v = O.adamw_update(g, p, m, v, sc)
-        return p, m, v, O.cast_bf16(p)
+def _oracle_steps(s, inputs, n_steps: int, barrier=None):
+    """Runs n_steps whole steps of the oracle, as it stands, on the scaled
+    workload: the sharded step over the state ranks' range (reduce-scatter,
+    AdamW, bf16 cast, all-gather write), the persistent group, and a forward
+    and a backward gather of every submodule.  Returns per-step seconds."""
+    import numpy as np
+    import oracle as O
+    plan = O.partition(s.numels, s.submodule_of, s.n_ranks, s.threshold, s.bucket)
+    st, full, ps = O.init_state(plan, inputs["mf"], inputs["mp"])
+    G = [inputs["G"][q] for q in range(plan.n_ranks)]
+    PG = [inputs["PG"][q] for q in range(plan.n_ranks)]
+    hi = int(inputs["hi"])
+    order = list(range(plan.n_submodules))
+    out = []
+    for t in range(1, n_steps + 1):
+        if barrier is not None:
+            barrier.wait()
+        t0 = time.perf_counter()
+        for k in order:
+            O.fetch_submodule(plan, k, st.sparam, ps.param)
+        for k in reversed(order):
+            O.fetch_submodule(plan, k, st.sparam, ps.param)
+        O.sharded_step(plan, s.hparams, t, G, st, full, 0, hi)
+        O.persistent_step(plan, s.hparams, t, PG, ps)
+        out.append(time.perf_counter() - t0)
+    del np
+    return out
 
-    t0 = time.perf_counter()
-    p, m, v, _ = one(1, p, m, v)
-    dt1 = time.perf_counter() - t0
-    reps = max(1, int(budget_s / max(dt1, 1e-3)))
-    t0 = time.perf_counter()
-    for t in range(2, 2 + reps):
-        p, m, v, _ = one(t, p, m, v)
-    dt = time.perf_counter() - t0
-    rate = rng_n * reps / dt
-    return rate, (f"{rng_n} consecutive elements of rank 0's shard, all {plan.n_ranks} ranks' "
-                  f"gradients, {reps} steps (numpy, one thread)"), dt
+
+def _cpu_worker(s, path, n_steps, barrier, q, wid):
+    import numpy as np
+    with np.load(path) as z:
+        inputs = {k: z[k] for k in z.files}
+    q.put((wid, _oracle_steps(s, inputs, n_steps, barrier)))
+
+
+def oracle_on_cores(s, inputs, n_steps: int, procs: int):
+    """The oracle's steps on `procs` host cores at once: procs independent
+    copies of the scaled step in spawned processes (one thread each),
+    started together at every step.  Returns per-step seconds (the slowest
+    process of each step)."""
+    import multiprocessing as mp
+    import numpy as np
+    if procs <= 1:
+        return _oracle_steps(s, inputs, n_steps)
+    fd, path = tempfile.mkstemp(suffix=".npz")
+    os.close(fd)
+    np.savez(path, **inputs)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = "1"
+    ctx = mp.get_context("spawn")
+    barrier, q = ctx.Barrier(procs), ctx.Queue()
+    ps = [ctx.Process(target=_cpu_worker, args=(s, path, n_steps, barrier, q, i))
+          for i in range(procs)]
+    for p in ps:
+        p.start()
+    res = dict(q.get() for _ in ps)
+    for p in ps:
+        p.join()
+    os.unlink(path)
+    return [max(res[i][k] for i in res) for k in range(n_steps)]
+
+
+def host_cores():
+    try:
+        aff = len(os.sched_getaffinity(0))
+    except AttributeError:
+        aff = os.cpu_count() or 1
+    return os.cpu_count() or 1, aff
+
+
+def cpu_oracle_baseline(w, view_rank0: bool, budget_s: float, target_params: int = 2_000_000):
+    """The CPU oracle, as it stands, timed on this host's cores: one whole
+    step (forward and backward gathers of every submodule, the sharded step
+    over the state ranks' range, the persistent group) of the same list
+    scaled down to about target_params parameters, single-threaded and on
+    every core at once.  params/s = the scaled step's parameters (times the
+    processes) / its measured time."""
+    s, f = scaled_workload(w, target_params)
+    inputs = _oracle_inputs(s, view_rank0)
+    import oracle as O
+    plan = O.partition(s.numels, s.submodule_of, s.n_ranks, s.threshold, s.bucket)
+    params = (plan.shard_len + plan.psi_s) if view_rank0 else s.psi
+    one = _oracle_steps(s, inputs, 1)[0]
+    n_steps = max(2, min(200, int(budget_s / max(one, 1e-3))))
+    single = _oracle_steps(s, inputs, n_steps)
+    nproc, aff = host_cores()
+    multi = oracle_on_cores(s, inputs, n_steps, aff)
+    v1 = params / statistics.mean(single)
+    vn = aff * params / statistics.mean(multi)
+    return {
+        "value": vn, "unit": "params/s", "cores": aff, "kind": "oracle",
+        "value_single_thread": v1, "cores_single": 1, "nproc": nproc, "affinity_cores": aff,
+        "ms_per_sample_step_single": statistics.mean(single) * 1e3,
+        "ms_per_sample_step_all_cores": statistics.mean(multi) * 1e3,
+        "sample": (f"the oracle's whole step on the same list scaled by f={f:.3g} "
+                   f"({params} params: {len(s.numels)} tensors, same N_d={s.n_ranks}, "
+                   f"persistent set and submodules); {n_steps} steps single-threaded, then "
+                   f"{aff} processes x {n_steps} steps at once (numpy, one thread each)"),
+    }
 
 
 def run_reference(args):
-    import numpy as np  # noqa: F401
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     import oracle as O
     w = make_workload(args)
+    view = WORKLOADS[args.workload][1] is not None
     plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
-    n_flat = plan.psi_pad if WORKLOADS[args.workload][1] is None else plan.shard_len
+    n_flat = plan.shard_len if view else plan.psi_pad
     config = step_config(args, w, args.gpus, plan.psi_pad, plan.psi_s, n_flat,
                          [plan.submodule_numel(k) for k in range(plan.n_submodules)])
-    budget = 4.0
-    rates = []
-    desc = None
-    for i in range(args.warmup + args.steps):
-        r, desc, _ = cpu_oracle_rate(make_workload(args), budget_s=budget)
-        if i >= args.warmup:
-            rates.append(r)
-    value = sum(rates) / len(rates)
+    s, f = scaled_workload(w, 2_000_000)
+    inputs = _oracle_inputs(s, view)
+    sp = O.partition(s.numels, s.submodule_of, s.n_ranks, s.threshold, s.bucket)
+    params = (sp.shard_len + sp.psi_s) if view else s.psi
+    nproc, aff = host_cores()
+    dts = oracle_on_cores(s, inputs, args.warmup + args.steps, aff)[args.warmup:]
+    ms = statistics.mean(dts) * 1e3 if dts else float("nan")
+    value = aff * params / (ms / 1e3)
+    cpu = {"value": value, "unit": "params/s", "cores": aff, "kind": "oracle", "nproc": nproc,
+           "sample": (f"the oracle's whole step on the same list scaled by f={f:.3g} "
+                      f"({params} params), {aff} processes at once (numpy, one thread each)")}
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        # the oracle's time for one whole step of the workload, extrapolated
-        # from the sample's rate
-        "ms_per_step": config["params"] / value * 1e3,
+        # measured: one step of what ran (every core's scaled step)
+        "ms_per_step": ms,
+        # the oracle's time for one whole step of the full-size workload at
+        # the same rate (not timed)
+        "extrapolated_ms_per_full_step": config["params"] / value * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": config,
-        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": cpu,
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -285,21 +450,26 @@ def replica_throughput(world: int, params_per_replica: int, ms_per_step: float) 
     return world * params_per_replica / (ms_per_step / 1e3)
 
 
-def launches_per_step(e) -> int:
-    """Kernel launches of one full step, counted from the plan: the fused
-    kernel once per gradient chunk, the persistent group once, and each
-    submodule gather ceil(pieces / 64) times, twice (forward, backward)."""
-    import math
+def submodule_pieces(e, k) -> int:
+    pieces = 0
+    for t, sub in enumerate(e.w.submodule_of):
+        if sub != k or e.w.numels[t] == 0:
+            continue
+        ti = e.plan.tensor(t)
+        pieces += 1 if ti.persistent else ti.n_segments
+    return pieces
+
+
+def gather_launches(e, bucket) -> int:
+    """Launches of the two gather passes: per zero3_fetch_submodules call
+    (one bucket) its pieces in launches of up to 512 (64 when they all fit
+    the small description)."""
     n = 0
-    for k in range(e.plan.info.n_submodules):
-        pieces = 0
-        for t, sub in enumerate(e.w.submodule_of):
-            if sub != k or e.w.numels[t] == 0:
-                continue
-            ti = e.plan.tensor(t)
-            pieces += 1 if ti.persistent else ti.n_segments
-        n += 2 * math.ceil(pieces / 64)
-    return n + len(e.chunks) + (1 if e.psi_s > 0 else 0)
+    for g in gather_groups([e.plan.submodule(k)[1] for k in range(e.plan.info.n_submodules)],
+                           bucket):
+        p = sum(submodule_pieces(e, k) for k in g)
+        n += 2 * (math.ceil(p / 512) if p > 64 else (1 if p > 0 else 0))
+    return n
 
 
 def setup_single(args, stream=None, **emu_kw):
@@ -605,6 +775,143 @@ def run_unfused(args):
     return 0
 
 
+def measure(args, name, world, local, with_e2e, with_cpu):
+    """The step of workload `name` on this GPU: device-resident timing
+    (every row by CUDA events on the launching stream, clocks sampled during
+    the timed region), the end-to-end variant through the C ABI with host
+    buffers, and the CPU oracle baseline.  Returns the line's fields."""
+    import torch
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+
+    fac, state_ranks, bucketed, _ = WORKLOADS[name]
+    w = make_workload(args, name)
+    stream = torch.cuda.Stream()
+    e = Emulation(w, device=f"cuda:{local}", state_ranks=state_ranks, bucketed=bucketed,
+                  stream=stream)
+    with torch.cuda.stream(stream):
+        e.init_params()
+        e.fill_grads(1)   # generated once before timing, reused by every step
+    torch.cuda.synchronize()
+    nbytes = e.step_bytes()
+    n_params = w.psi if state_ranks is None else nbytes["flat_elems"] + e.psi_s
+    bucket = w.gather_bucket
+
+    def full_step(t, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        e.forward_backward_gathers(bucket=bucket)
+        if ev is not None:
+            ev[1].record(stream)
+        # the persistent group rides in the first chunk's launch
+        for c, ((a_, b_), G) in enumerate(zip(e.chunks, e.grads)):
+            zero3.zero3_step(e.plan, e.hp, t, e.ptrs(G), a_, e.ptrs(e.master), e.ptrs(e.m),
+                             e.ptrs(e.v), e.ptrs(e.sparam), e.full.data_ptr(),
+                             e.persist if c == 0 else None, a_, b_, e.sid)
+        if ev is not None:
+            ev[2].record(stream)
+
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        full_step(t)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    tw0 = time.time()
+    wall0 = time.perf_counter()
+    start.record(stream)
+    for k in range(args.steps):
+        t += 1
+        full_step(t, evs[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    tw1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms = start.elapsed_time(end) / args.steps
+    gather_ms = [x[0].elapsed_time(x[1]) for x in evs]
+    fused_ms = [x[1].elapsed_time(x[2]) for x in evs]
+    clk = clocks.stop(tw0, tw1)
+    if world > 1:
+        ms = reduce_max(ms, f"cuda:{local}")
+
+    e2e = None
+    if with_e2e:
+        e2e = run_e2e(e, w, args, stream, n_params, t)
+        if world > 1 and e2e is not None and e2e.get("ms_per_step"):
+            e2e["ms_per_step"] = reduce_max(e2e["ms_per_step"], f"cuda:{local}")
+            e2e["value"] = replica_throughput(world, n_params, e2e["ms_per_step"])
+
+    n_fused = max(len(e.chunks), 1)
+    fused_bytes = nbytes["fused"] + nbytes["persistent"]
+    fused_launch_ms = statistics.mean(fused_ms) / n_fused
+    peak, peak_kind = peaks()
+    achieved = fused_bytes / n_fused / (fused_launch_ms / 1e3) / 1e9
+    n_gather = gather_launches(e, bucket)
+    cpu = None
+    if with_cpu:
+        cpu = cpu_oracle_baseline(w, state_ranks is not None, args.cpu_budget)
+    step_gbs = nbytes["total"] / (ms / 1e3) / 1e9
+    sha = kernels_sha()
+    traffic = None if args.n_ranks else profile_traffic(name, sha)
+    res = {
+        "value": replica_throughput(world, n_params, ms),
+        "unit": "params/s",
+        "ms_per_step": ms,
+        "config": step_config(args, w, world, e.psi_pad, e.psi_s, nbytes["flat_elems"],
+                              [e.plan.submodule(k)[1] for k in range(e.plan.info.n_submodules)],
+                              name=name),
+        "step_gbs": step_gbs,
+        "step_hbm_frac": step_gbs / peak,
+        "fused_step": {"ms_per_launch": fused_launch_ms, "launches_per_step": n_fused,
+                       "bytes_per_launch": fused_bytes / n_fused,
+                       "bytes_per_elem": 2 * w.n_ranks + 28,
+                       "gbs": achieved, "frac": achieved / peak,
+                       "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                       "params_per_s": (nbytes["flat_elems"] + e.psi_s) / n_fused
+                       / (fused_launch_ms / 1e3)},
+        # every row of the step, timed by events on the launching stream,
+        # against the same measured copy peak as the roofline
+        "rows": {
+            nm: dict(ms_per_step=ms_, launches=n_, bytes=b_,
+                     gbs=b_ / ms_ / 1e6 if ms_ > 0 else 0.0,
+                     frac=b_ / ms_ / 1e6 / peak if ms_ > 0 else 0.0)
+            for nm, ms_, n_, b_ in (
+                ("a1_a4_fused", statistics.mean(fused_ms), n_fused, fused_bytes),
+                ("a5_gathers", statistics.mean(gather_ms), n_gather, nbytes["gathers"]))
+        },
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "peak_note": "MEASURED_PEAKS.json hbm_gbs: a torch copy, read+write bytes",
+                     "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                     "nominal_peak": NOMINAL_HBM_GBS,
+                     "nominal_note": "GB300 HBM3e nominal bandwidth (NVIDIA product figure)",
+                     "traffic": traffic,
+                     "traffic_source": (os.path.relpath(PROFILE_JSON, ROOT) + f" (kernels.cu "
+                                        f"{sha})") if traffic is not None else None,
+                     "kernel": "stream_kernel<kFused, N_d> (zero3_step)"},
+        "gpu_launches": (n_fused + n_gather) * args.steps,
+        "clocks": clk,
+        "wall_s_timed": wall,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+    }
+    del e
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -620,135 +927,25 @@ def run_ours(args):
         b.build_all(quiet=True)
     if world > 1:
         dist.barrier()
-    from zero_sharded_optimizer_shard_gb300 import workloads as W, zero3
-    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
 
-    fac, state_ranks, bucketed, _ = WORKLOADS[args.workload]
-    w = make_workload(args)
-    stream = torch.cuda.Stream()
-    e = Emulation(w, device=f"cuda:{local}", state_ranks=state_ranks, bucketed=bucketed,
-                  stream=stream)
-    with torch.cuda.stream(stream):
-        e.init_params()
-        e.fill_grads(1)   # generated once before timing, reused by every step
-    torch.cuda.synchronize()
-    nbytes = e.step_bytes()
-    n_params = w.psi if state_ranks is None else nbytes["flat_elems"] + e.psi_s
-
-    def full_step(t, ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        e.forward_backward_gathers()
-        if ev is not None:
-            ev[1].record(stream)
-        for (a_, b_), G in zip(e.chunks, e.grads):
-            zero3.zero3_step(e.plan, e.hp, t, e.ptrs(G), a_, e.ptrs(e.master), e.ptrs(e.m),
-                             e.ptrs(e.v), e.ptrs(e.sparam), e.full.data_ptr(), None, a_, b_, e.sid)
-        if ev is not None:
-            ev[2].record(stream)
-        zero3.zero3_persistent_step(e.plan, e.hp, t, e.persist, e.sid)
-        if ev is not None:
-            ev[3].record(stream)
-
-    t = 0
-    for _ in range(args.warmup):
-        t += 1
-        full_step(t)
-    torch.cuda.synchronize()
-
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.5)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    tw0 = time.time()
-    wall0 = time.perf_counter()
-    start.record(stream)
-    for k in range(args.steps):
-        t += 1
-        full_step(t, evs[k])
-    end.record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    tw1 = time.time()
-    if world > 1:
-        dist.barrier()
-    ms = start.elapsed_time(end)
-    gather_ms = [x[0].elapsed_time(x[1]) for x in evs]
-    fused_ms = [x[1].elapsed_time(x[2]) for x in evs]
-    persist_ms = [x[2].elapsed_time(x[3]) for x in evs]
-    clk = clocks.stop(tw0, tw1)
-    if world > 1:
-        ms = reduce_max(ms, f"cuda:{local}")
-
-    # ---- end to end through the public API: host gradients in, params out
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(e, w, args, stream, n_params, t)
-        if world > 1 and e2e is not None and e2e.get("ms_per_step"):
-            e2e["ms_per_step"] = reduce_max(e2e["ms_per_step"], f"cuda:{local}")
-            e2e["value"] = replica_throughput(world, n_params, e2e["ms_per_step"])
-
+    head = measure(args, args.workload, world, local, with_e2e=not args.no_e2e,
+                   with_cpu=(not args.no_cpu_baseline and world == 1 and rank == 0))
+    extra = {}
+    second = second_workload(args)
+    if second:
+        # the host-copy variant of the second workload runs at N = 1 only (its
+        # pinned host buffers would be held by every replica at once)
+        extra[second] = measure(args, second, world, local,
+                                with_e2e=(not args.no_e2e and world == 1),
+                                with_cpu=(not args.no_cpu_baseline and world == 1 and rank == 0))
     if rank == 0:
-        ms_step = ms / args.steps
-        fused_launch_ms = statistics.mean(fused_ms) / max(len(e.chunks), 1)
-        fused_bytes_launch = nbytes["fused"] / max(len(e.chunks), 1)
-        peak, peak_kind = peaks()
-        achieved = fused_bytes_launch / (fused_launch_ms / 1e3) / 1e9
-        cpu = None
-        if not args.no_cpu_baseline and world == 1:
-            rate, sample, _ = cpu_oracle_rate(w, budget_s=15.0)
-            cpu = {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
-                   "sample": sample}
-        step_gbs = nbytes["total"] / (ms_step / 1e3) / 1e9
-        line = {
-            "metric": METRIC,
-            "value": replica_throughput(world, n_params, ms_step),
-            "unit": "params/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms_step,
-            "higher_is_better": True,
-            "scaling": "weak",
-            "vs_baseline": None,
-            "dtype": "f32",
-            "data": "synthetic",
-            "config": step_config(args, w, world, e.psi_pad, e.psi_s, nbytes["flat_elems"],
-                                  [e.plan.submodule(k)[1]
-                                   for k in range(e.plan.info.n_submodules)]),
-            "step_gbs": step_gbs,
-            "step_hbm_frac": step_gbs / peak,
-            "fused_step": {"ms_per_launch": fused_launch_ms, "launches_per_step": len(e.chunks),
-                           "bytes_per_launch": fused_bytes_launch,
-                           "bytes_per_elem": 2 * w.n_ranks + 28,
-                           "params_per_s": nbytes["flat_elems"] / max(len(e.chunks), 1)
-                           / (fused_launch_ms / 1e3)},
-            # every row of the step, timed by events on the launching stream,
-            # against the same measured copy peak as the roofline
-            "rows": {
-                name: dict(ms_per_step=ms_, launches=n_, bytes=b_,
-                           gbs=b_ / ms_ / 1e6 if ms_ > 0 else 0.0,
-                           frac=b_ / ms_ / 1e6 / peak if ms_ > 0 else 0.0)
-                for name, ms_, n_, b_ in (
-                    ("a1_a3_fused", statistics.mean(fused_ms), len(e.chunks), nbytes["fused"]),
-                    ("a4_persistent", statistics.mean(persist_ms), 1, nbytes["persistent"]),
-                    ("a5_gathers", statistics.mean(gather_ms),
-                     launches_per_step(e) - len(e.chunks) - (1 if e.psi_s > 0 else 0),
-                     nbytes["gathers"]))
-            },
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": profile_traffic(kernels_sha())
-                         if (args.workload == "decoder_1p3b" and not args.n_ranks) else None,
-                         "kernel": "stream_kernel<kFused, N_d> (zero3_step)"},
-            "gpu_launches": launches_per_step(e) * args.steps,
-            "clocks": clk,
-            "wall_s_timed": wall,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-        }
+        line = {"metric": METRIC, "value": head["value"], "unit": "params/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic"}
+        line.update({k: v for k, v in head.items() if k not in line})
+        if extra:
+            line["configs"] = extra
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
@@ -758,13 +955,17 @@ def run_ours(args):
 def run_e2e(e, w, args, stream, n_params, t0):
     """Same step through the public API with host buffers: every step copies
     every rank's local gradients (and the persistent-group gradients) from
-    pinned host memory and reads the full bf16 parameter buffer back into
-    pinned host memory.  Pipelined over two device buffer sets: the upload of
-    step k+1 and the read-back of step k run on their own streams while step
-    k computes; events order every reuse of a buffer."""
+    pinned host memory and reads the parameters the step updated (the state
+    ranks' range of the full bf16 buffer) back into pinned host memory.
+    Pipelined over two device buffer sets: the upload of step k+1 and the
+    read-back of step k run on their own streams while step k computes;
+    events order every reuse of a buffer.  Before the pipelined run, the
+    same copies alone measure the host link (one copy per buffer)."""
     import torch
     from zero_sharded_optimizer_shard_gb300 import zero3
     steps = max(2, min(args.steps, 6))
+    lo = min(e.state_ranks) * e.S
+    hi = min((max(e.state_ranks) + 1) * e.S, e.psi_pad)
     need = sum(x.numel() * 2 for G in e.grads for x in G) + e.full.numel() * 2
     free, _ = torch.cuda.mem_get_info()
     if need > free - (2 << 30):
@@ -773,7 +974,7 @@ def run_e2e(e, w, args, stream, n_params, t0):
     try:
         host_g = [[torch.empty(x.numel(), dtype=x.dtype, pin_memory=True) for x in G] for G in e.grads]
         host_pg = [torch.empty(x.numel(), dtype=x.dtype, pin_memory=True) for x in e.pgrads]
-        host_full = torch.empty(e.full.numel(), dtype=e.full.dtype, pin_memory=True)
+        host_full = torch.empty(hi - lo, dtype=e.full.dtype, pin_memory=True)
         dev_g = [e.grads, [[torch.empty_like(x) for x in G] for G in e.grads]]
         dev_pg = [e.pgrads, [torch.empty_like(x) for x in e.pgrads]]
         dev_full = [e.full, torch.empty_like(e.full)]
@@ -787,6 +988,30 @@ def run_e2e(e, w, args, stream, n_params, t0):
     h2d = sum(x.numel() * 2 for hG in host_g for x in hG) + sum(x.numel() * 2 for x in host_pg)
     d2h = host_full.numel() * 2
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def upload(b):
+        for hG, G in zip(host_g, dev_g[b]):
+            for h, d in zip(hG, G):
+                d.copy_(h, non_blocking=True)
+        for h, d in zip(host_pg, dev_pg[b]):
+            d.copy_(h, non_blocking=True)
+
+    # the host link alone: the same uploads and read-back, nothing else running
+    link = {}
+    torch.cuda.synchronize()
+    for nm, fn, st_, nb in (("h2d", lambda: upload(1), up, h2d),
+                            ("d2h", lambda: host_full.copy_(dev_full[1][lo:hi], non_blocking=True),
+                             down, d2h)):
+        ts = []
+        for _ in range(2):
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(st_):
+                a_.record(st_)
+                fn()
+                b_.record(st_)
+            torch.cuda.synchronize()
+            ts.append(a_.elapsed_time(b_))
+        link[nm] = nb / (min(ts) / 1e3) / 1e9
     ev = lambda: torch.cuda.Event()
     uploaded = [ev() for _ in range(steps)]
     up_t = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -804,40 +1029,41 @@ def run_e2e(e, w, args, stream, n_params, t0):
             if k >= 2:
                 up.wait_event(computed[k - 2])  # buffer set b was read by step k-2
             up_t[k][0].record(up)
-            for hG, G in zip(host_g, dev_g[b]):
-                for h, d in zip(hG, G):
-                    d.copy_(h, non_blocking=True)
-            for h, d in zip(host_pg, dev_pg[b]):
-                d.copy_(h, non_blocking=True)
+            upload(b)
             up_t[k][1].record(up)
             uploaded[k].record(up)
         stream.wait_event(uploaded[k])
         if k >= 2:
             stream.wait_event(read[k - 2])      # full[b] of step k-2 was read back
         t += 1
-        e.forward_backward_gathers()
+        e.forward_backward_gathers(bucket=w.gather_bucket)
         ps = zero3.persist_state([x.data_ptr() for x in dev_pg[b]], e.pmaster.data_ptr(),
                                  e.pm.data_ptr(), e.pv.data_ptr(), e.pparam.data_ptr())
-        for (lo, hi), G in zip(e.chunks, dev_g[b]):
-            zero3.zero3_step(e.plan, e.hp, t, e.ptrs(G), lo, e.ptrs(e.master), e.ptrs(e.m),
-                             e.ptrs(e.v), e.ptrs(e.sparam), dev_full[b].data_ptr(), None, lo, hi,
-                             e.sid)
-        zero3.zero3_persistent_step(e.plan, e.hp, t, ps, e.sid)
+        for c, ((clo, chi), G) in enumerate(zip(e.chunks, dev_g[b])):
+            zero3.zero3_step(e.plan, e.hp, t, e.ptrs(G), clo, e.ptrs(e.master), e.ptrs(e.m),
+                             e.ptrs(e.v), e.ptrs(e.sparam), dev_full[b].data_ptr(),
+                             ps if c == 0 else None, clo, chi, e.sid)
         computed[k].record(stream)
         with torch.cuda.stream(down):
             down.wait_event(computed[k])
-            host_full.copy_(dev_full[b], non_blocking=True)
+            host_full.copy_(dev_full[b][lo:hi], non_blocking=True)
             read[k].record(down)
     end.record(down)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     ms = start.elapsed_time(end) / steps
-    up_ms = [a.elapsed_time(b_) for a, b_ in up_t]
+    up_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in up_t)
+    h2d_gbs = h2d / (up_ms / 1e3) / 1e9
     return {"value": n_params / (ms / 1e3), "unit": "params/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms,
             "wall_ms_per_step": wall * 1e3 / steps,
-            "upload_ms_per_step": statistics.mean(up_ms),
-            "h2d_gbs": h2d / (statistics.mean(up_ms) / 1e3) / 1e9,
+            "upload_ms_per_step": up_ms,
+            "h2d_gbs": h2d_gbs,
+            "h2d_link_gbs": link["h2d"], "d2h_link_gbs": link["d2h"],
+            "h2d_frac": h2d_gbs / link["h2d"],
+            "bound_ms_per_step": max(h2d / link["h2d"], d2h / link["d2h"]) / 1e6,
+            "link_note": "host link measured in the same run: the same pinned buffers copied "
+                         "alone, one copy per buffer, best of 2",
             "pipeline": "uploads of step k+1 and read-back of step k overlap step k"}
 
 

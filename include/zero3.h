@@ -220,7 +220,7 @@ zero3_status zero3_allgather(const zero3_plan* plan, const uint16_t* const* spar
  * Results equal zero3_reduce_scatter(F32) + zero3_adamw_step(F32) +
  * zero3_allgather bit for bit.  If persist is not NULL the persistent group is
  * also updated (same arithmetic, DDP style, on its single resident copy),
- * whatever the range. */
+ * whatever the range, in the same kernel launch: one launch per call. */
 zero3_status zero3_step(const zero3_plan* plan, const zero3_adamw_hparams* hp, int64_t t,
                         const uint16_t* const* grads, int64_t grads_origin,
                         float* const* master, float* const* m, float* const* v,
@@ -320,6 +320,26 @@ zero3_status zero3_cast_params(const zero3_plan* plan, const float* const* maste
 zero3_status zero3_fetch_submodule(zero3_plan* plan, int32_t k, const uint16_t* const* sparam,
                                    const uint16_t* persist_param, uint16_t* out,
                                    zero3_stream stream);
+
+/* Several fetches in one call, their gathers packed into shared launches
+ * ([cnhsyj] section 3.1, allgather_bucket_size: many small gathers are
+ * aggregated into a few large ones; [hotelren], minimal ZeRO-3 config,
+ * allgather_bucket_size 5e8).  The result equals n calls
+ * zero3_fetch_submodule(ks[i], ..., outs[i]) in list order: every submodule
+ * keeps its own ZeroParamStatus transitions, reference count and event, and a
+ * submodule listed twice, or already fetched, only gains a reference and must
+ * name the same output (ZERO3_ESTATE otherwise).  The gathers of the
+ * submodules that were NOT_AVAILABLE run as launches of up to 512 pieces
+ * (one piece per tensor segment), so a bucket of many small submodules costs
+ * a few launches instead of one per submodule.
+ * ks: host array of n submodule ids; outs: host array of n device pointers
+ * (16-byte aligned, each holding its submodule's elements; outputs of
+ * different submodules must not overlap).  Everything is checked before
+ * anything is launched or any state changes: EINVAL (bad id, NULL or
+ * misaligned pointer, n < 0), ESTATE, ECUDA, ENOMEM. */
+zero3_status zero3_fetch_submodules(zero3_plan* plan, const int32_t* ks, int32_t n,
+                                    const uint16_t* const* sparam, const uint16_t* persist_param,
+                                    uint16_t* const* outs, zero3_stream stream);
 
 /* Drops one reference; at zero the submodule returns to NOT_AVAILABLE (its
  * gathered copy may be reused by the caller).  ZERO3_ESTATE if the submodule

@@ -220,6 +220,28 @@ def test_submodule_state_errors_on_host(lib):
     assert zero3.zero3_submodule_status(p, 0) == zero3.NOT_AVAILABLE
 
 
+def test_fetch_submodules_rejects_bad_arguments_on_host(lib):
+    """The multi-submodule fetch checks every listed submodule before it
+    launches anything or changes any state (fake device pointers: a launch
+    would fault, so none may happen)."""
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    p = _plan()
+    P = zero3._ptrs
+    ks = (C.c_int32 * 3)(0, 1, 2)
+    E = zero3.EINVAL
+    f = lambda k, n, sp, outs: zero3.raw_status("zero3_fetch_submodules", p.handle, k, n, sp, FAKE,
+                                                outs, None)
+    assert f(ks, 2, P([FAKE, FAKE]), P([FAKE, MISALIGNED])) == E     # second output misaligned
+    assert f(ks, 3, P([FAKE, FAKE]), P([FAKE, FAKE, FAKE])) == E     # id 2 out of range
+    assert f(ks, -1, P([FAKE, FAKE]), P([FAKE])) == E
+    assert f(ks, 2, P([FAKE, FAKE]), None) == E
+    assert f(None, 2, P([FAKE, FAKE]), P([FAKE, FAKE])) == E
+    assert f(ks, 2, P([FAKE, 0]), P([FAKE, FAKE])) == E              # a missing owner shard
+    assert f(None, 0, None, None) == zero3.OK                         # nothing to do
+    for k in (0, 1):
+        assert zero3.zero3_submodule_status(p, k) == zero3.NOT_AVAILABLE
+
+
 def test_status_strings(lib):
     from zero_sharded_optimizer_shard_gb300 import zero3
     assert zero3.status_string(zero3.OK) == "ok"

@@ -4,6 +4,7 @@ import json
 import os
 import subprocess
 import sys
+import time
 
 import pytest
 
@@ -23,14 +24,36 @@ def run_bench(*args, timeout=600):
 
 
 def test_reference_arm_line():
-    d = run_bench("--impl", "reference", "--workload", "gpt2_small", "--steps", "1",
-                  "--warmup", "0")
+    t0 = time.time()
+    d = run_bench("--impl", "reference", "--workload", "gpt2_small", "--steps", "2",
+                  "--warmup", "1")
+    wall = time.time() - t0
     assert BASE_KEYS <= set(d) and d["impl"] == "reference"
     assert d["unit"] == "params/s" and d["value"] > 0 and d["higher_is_better"] is True
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    cpu = d["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["nproc"] >= cpu["cores"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["config"]["workload"] and d["config"]["bytes_per_step"] > 0
-    assert d["ms_per_step"] > 0
+    # ms_per_step is what was timed: the timed steps fit in the run's own wall clock
+    assert 0 < d["ms_per_step"] and d["steps"] * d["ms_per_step"] / 1e3 < wall
+    assert d["extrapolated_ms_per_full_step"] > d["ms_per_step"]
+
+
+def test_scaled_oracle_sample_keeps_the_partition_shape():
+    """The CPU baseline's sample is the same list scaled down: same tensor
+    count, same persistent set, same submodules and N_d."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle as O
+    from zero_sharded_optimizer_shard_gb300 import workloads as W
+    for w in (W.decoder_1p3b(), W.llama_7b(), W.ragged(), W.gpt2_small()):
+        s, f = bench.scaled_workload(w, 2_000_000)
+        assert 0 < f < 1 and len(s.numels) == len(w.numels)
+        assert abs(s.psi - 2_000_000) / 2_000_000 < 0.2
+        a = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+        b = O.partition(s.numels, s.submodule_of, s.n_ranks, s.threshold, s.bucket)
+        assert a.persistent == b.persistent and a.n_submodules == b.n_submodules
+        assert [x == 0 for x in w.numels] == [x == 0 for x in s.numels]
 
 
 @pytest.mark.gpu
@@ -46,9 +69,15 @@ def test_our_arm_line():
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] > 0 and {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
     rows = d["rows"]
-    assert set(rows) == {"a1_a3_fused", "a4_persistent", "a5_gathers"}
-    assert all(0 < r["frac"] < 2 and r["launches"] >= 1 for r in rows.values())
-    assert rows["a1_a3_fused"]["frac"] == pytest.approx(r["frac"], rel=1e-6)
+    assert set(rows) == {"a1_a4_fused", "a5_gathers"}
+    assert all(0 < x["frac"] < 2 and x["launches"] >= 1 for x in rows.values())
+    assert rows["a1_a4_fused"]["frac"] == pytest.approx(r["frac"], rel=1e-6)
+    assert rows["a1_a4_fused"]["launches"] == 1  # persistent group in the same launch
+    assert 0 < r["frac_of_nominal"] < r["frac"]
+    cpu = d["cpu_baseline"]
+    assert cpu["value_single_thread"] > 0 and cpu["nproc"] >= cpu["cores"] >= 1
+    assert e["h2d_link_gbs"] > 0 and e["d2h_link_gbs"] > 0 and 0 < e["h2d_frac"] < 1.5
+    assert "configs" not in d  # no second workload after gpt2_small by default
     # the reference arm reports the same workload description
     ref = run_bench("--impl", "reference", "--workload", "gpt2_small", "--steps", "1",
                     "--warmup", "0")
@@ -82,3 +111,15 @@ def test_arms_describe_the_same_workload(workload, lib):
                              info.shard_len if view else info.psi_pad,
                              [plan.submodule(k)[1] for k in range(info.n_submodules)])
     assert ours == ref
+
+
+@pytest.mark.gpu
+def test_second_workload_in_the_same_line():
+    """A second workload is measured in the same run and reported under
+    `configs` with its own roofline, rows, CPU baseline and e2e."""
+    d = run_bench("--workload", "gpt2_small", "--second", "ragged", "--steps", "3",
+                  "--warmup", "3", "--cpu-budget", "1")
+    c = d["configs"]["ragged"]
+    assert c["config"]["name"] == "ragged" and c["value"] > 0
+    assert 0 < c["roofline"]["frac"] < 2 and c["cpu_baseline"]["value"] > 0
+    assert c["e2e"]["value"] > 0 and set(c["rows"]) == {"a1_a4_fused", "a5_gathers"}

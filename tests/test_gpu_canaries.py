@@ -41,6 +41,10 @@ def test_every_writer_stays_in_bounds(wname, tmp_path):
     ok(e, "fused step + persistent (bucketed)")
     e.forward_backward_gathers()
     ok(e, "submodule gathers")
+    total = sum(e.plan.submodule(k)[1] for k in range(e.plan.info.n_submodules))
+    for div in (1, 4):  # every submodule in one call; buckets of a few
+        e.forward_backward_gathers(bucket=max(1, total // div))
+    ok(e, "bucketed submodule gathers (guarded arena)")
     nd, S = e.nd, e.S
     # unfused stages into guarded shard-gradient buffers, both dtypes
     for dt, torch_dt in ((zero3.F32, torch.float32), (zero3.BF16, torch.bfloat16)):

@@ -2,6 +2,8 @@
 // range, the submodule state machine, and the launches.
 #include <cmath>
 #include <cstring>
+#include <new>
+#include <vector>
 
 #include "internal.h"
 
@@ -140,6 +142,26 @@ bool persist_ok(const zero3_plan* p, const zero3_persist_state* ps) {
            aligned16(ps->master) && aligned16(ps->m) && aligned16(ps->v) && aligned16(ps->param);
 }
 
+// Appends the persistent group to a fused launch as one more span: local
+// indices [0, psi_s) of its resident copy, gradients from the group's own
+// per-rank buffers (pgrads), no write to `full`.  The arithmetic per element
+// is the flat spans' (fixed-order sum times 1/N_d, AdamW, bf16 cast).
+void add_persistent_span(const zero3_plan* p, const zero3_persist_state* ps, StreamArgs& a) {
+    for (int q = 0; q < p->n_ranks; ++q) a.pgrads[q] = ps->grads[q];
+    Span s;
+    std::memset(&s, 0, sizeof(s));
+    s.lo = 0;
+    s.hi = p->psi_s;
+    s.gofs = 0;
+    s.fofs = -1;
+    s.pg = 1;
+    s.master = ps->master;
+    s.m = ps->m;
+    s.v = ps->v;
+    s.out = ps->param;
+    add_span(a, s);
+}
+
 zero3_status persistent_launch(const zero3_plan* p, const z3::Scalars& sc,
                                const zero3_persist_state* ps, cudaStream_t stream) {
     if (p->psi_s == 0) return ZERO3_OK;
@@ -148,18 +170,7 @@ zero3_status persistent_launch(const zero3_plan* p, const z3::Scalars& sc,
     std::memset(&a, 0, sizeof(a));
     a.nd = p->n_ranks;
     a.sc = sc;
-    for (int q = 0; q < p->n_ranks; ++q) a.grads[q] = ps->grads[q];
-    Span s;
-    std::memset(&s, 0, sizeof(s));
-    s.lo = 0;
-    s.hi = p->psi_s;
-    s.gofs = 0;
-    s.fofs = -1;
-    s.master = ps->master;
-    s.m = ps->m;
-    s.v = ps->v;
-    s.out = ps->param;
-    add_span(a, s);
+    add_persistent_span(p, ps, a);
     return cuda_status(z3::launch_stream(z3::kFused, a, stream));
 }
 
@@ -185,53 +196,139 @@ zero3_status check_gather_sources(const zero3_plan* p, int32_t k, const uint16_t
     return ZERO3_OK;
 }
 
-zero3_status gather_submodule(const zero3_plan* p, int32_t k, const uint16_t* const* sparam,
-                              const uint16_t* persist_param, uint16_t* out, cudaStream_t stream) {
-    // the kernel's chunks are 8-element units relative to `out`, stored 16
-    // bytes at a time: `out` must be 16-byte aligned
-    if (p->sub_numel[k] > 0 && (!out || !aligned16(out))) return ZERO3_EINVAL;
-    GatherArgs a;
-    std::memset(&a, 0, sizeof(a));
-    a.out = out;
-    int64_t running = 0;
-    auto flush = [&]() -> zero3_status {
-        zero3_status st = cuda_status(launch_gather(a, stream));
-        a.n_segs = 0;
-        a.total_chunks = 0;
-        return st;
-    };
-    auto push = [&](const uint16_t* src, int64_t dst_off, int64_t len) -> zero3_status {
-        if (len <= 0) return ZERO3_OK;
-        if (a.n_segs == kMaxGatherSegs) {
-            zero3_status st = flush();
-            if (st != ZERO3_OK) return st;
-        }
-        GatherSeg& g = a.seg[a.n_segs++];
-        g.src = src;
-        g.dst_off = dst_off;
-        g.len = len;
-        g.chunk0 = a.total_chunks;
-        // phase of the source element that lands on an aligned chunk of out
-        const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
-        g.sphase = static_cast<int32_t>(((sa - 2u * static_cast<uintptr_t>(dst_off)) % 16u) / 2u);
-        a.total_chunks += ((dst_off + len) - (dst_off & ~static_cast<int64_t>(7)) + 7) / 8;
-        return ZERO3_OK;
-    };
-    for (int64_t t : p->sub_tensors[k]) {
-        zero3_status st = ZERO3_OK;
-        if (p->persistent[t]) {
-            st = push(persist_param + p->offset[t], running, p->numel[t]);
-        } else {
-            for (int64_t s = p->seg_begin[t]; s < p->seg_begin[t + 1] && st == ZERO3_OK; ++s) {
-                const zero3_segment& sg = p->segs[s];
-                st = push(sparam[sg.rank] + sg.shard_off, running + sg.tensor_off, sg.len);
-            }
-        }
-        if (st != ZERO3_OK) return st;
-        running += p->numel[t];
+PieceLauncher::PieceLauncher(int kind, cudaStream_t stream, bool large)
+    : kind_(kind), stream_(stream), large_(large) {
+    if (large)
+        args_ = new (std::nothrow) PieceArgs<kLargePieces>;
+    else
+        args_ = new (std::nothrow) PieceArgs<kSmallPieces>;
+    if (args_) {
+        if (large)
+            static_cast<PieceArgs<kLargePieces>*>(args_)->n = 0;
+        else
+            static_cast<PieceArgs<kSmallPieces>*>(args_)->n = 0;
     }
-    if (a.n_segs > 0) return flush();
+}
+
+PieceLauncher::~PieceLauncher() {
+    if (large_)
+        delete static_cast<PieceArgs<kLargePieces>*>(args_);
+    else
+        delete static_cast<PieceArgs<kSmallPieces>*>(args_);
+}
+
+namespace {
+
+template <int MAXP>
+zero3_status piece_flush(PieceArgs<MAXP>& a, int kind, cudaStream_t stream, int64_t* launches,
+                         cudaError_t (*launch)(int, const PieceArgs<MAXP>&, cudaStream_t)) {
+    if (a.n == 0) return ZERO3_OK;
+    const cudaError_t e = launch(kind, a, stream);
+    a.n = 0;
+    if (e != cudaSuccess) return ZERO3_ECUDA;
+    *launches += 1;
     return ZERO3_OK;
+}
+
+// Appends one piece; flushes first when the description is full or the
+// launch's warp count would not fit its 32-bit numbering.
+template <int MAXP>
+zero3_status piece_add(PieceArgs<MAXP>& a, int kind, cudaStream_t stream, int64_t* launches,
+                       cudaError_t (*launch)(int, const PieceArgs<MAXP>&, cudaStream_t),
+                       const Piece& pc) {
+    const uint64_t chunks = static_cast<uint64_t>((pc.hi + 7) / 8);
+    const uint64_t warps = (chunks + kPieceWarpChunks - 1) / kPieceWarpChunks;
+    const uint64_t cap = 0xffffffffull - kPieceWarpChunks;  // room for the grid rounding
+    if (warps > cap) return ZERO3_EINVAL;  // a single piece beyond 2^41 elements
+    if (a.n == MAXP || (a.n > 0 && a.warp0[a.n] + warps > cap)) {
+        zero3_status st = piece_flush(a, kind, stream, launches, launch);
+        if (st != ZERO3_OK) return st;
+    }
+    if (a.n == 0) a.warp0[0] = 0;
+    a.piece[a.n] = pc;
+    a.warp0[a.n + 1] = a.warp0[a.n] + static_cast<uint32_t>(warps);
+    a.n += 1;
+    return ZERO3_OK;
+}
+
+}  // namespace
+
+zero3_status PieceLauncher::add(const void* src, const float* scales, int64_t src_index,
+                                uint16_t* dst, int64_t len) {
+    if (!args_) return ZERO3_ENOMEM;
+    if (len <= 0) return ZERO3_OK;
+    // destination base rounded down to 16 bytes; the piece starts at lo
+    const uintptr_t da = reinterpret_cast<uintptr_t>(dst);
+    const int64_t lo = static_cast<int64_t>((da >> 1) & 7u);
+    Piece pc;
+    std::memset(&pc, 0, sizeof(pc));
+    pc.src = src;
+    pc.scales = scales;
+    pc.dst = dst - lo;
+    pc.lo = lo;
+    pc.hi = lo + len;
+    pc.s0 = src_index - lo;
+    if (kind_ == kPieceBf16)  // element phase of the source at aligned destination chunks
+        pc.ph = static_cast<int32_t>(
+            (static_cast<int64_t>(reinterpret_cast<uintptr_t>(src) >> 1) + pc.s0) & 7);
+    else  // code buffers are 16-byte aligned: the phase is the source index's
+        pc.ph = static_cast<int32_t>(pc.s0 & 7);
+    if (large_)
+        return piece_add(*static_cast<PieceArgs<kLargePieces>*>(args_), kind_, stream_,
+                         &launches_, launch_pieces_large, pc);
+    return piece_add(*static_cast<PieceArgs<kSmallPieces>*>(args_), kind_, stream_, &launches_,
+                     launch_pieces_small, pc);
+}
+
+zero3_status PieceLauncher::flush() {
+    if (!args_) return ZERO3_ENOMEM;
+    if (large_)
+        return piece_flush(*static_cast<PieceArgs<kLargePieces>*>(args_), kind_, stream_,
+                           &launches_, launch_pieces_large);
+    return piece_flush(*static_cast<PieceArgs<kSmallPieces>*>(args_), kind_, stream_, &launches_,
+                       launch_pieces_small);
+}
+
+// Pieces of submodule k: each member tensor in list order, a persistent one
+// from its resident copy, a partitioned one segment by segment from the
+// owning shards.
+int64_t submodule_pieces(const zero3_plan* p, int32_t k) {
+    int64_t n = 0;
+    for (int64_t t : p->sub_tensors[k]) {
+        if (p->numel[t] == 0) continue;
+        n += p->persistent[t] ? 1 : p->seg_begin[t + 1] - p->seg_begin[t];
+    }
+    return n;
+}
+
+zero3_status gather_submodules(const zero3_plan* p, const int32_t* ks, int64_t n,
+                               const uint16_t* const* sparam, const uint16_t* persist_param,
+                               uint16_t* const* outs, cudaStream_t stream, int64_t* n_launches) {
+    int64_t pieces = 0;
+    for (int64_t i = 0; i < n; ++i) pieces += submodule_pieces(p, ks[i]);
+    PieceLauncher L(kPieceBf16, stream, pieces > kSmallPieces);
+    for (int64_t i = 0; i < n; ++i) {
+        const int32_t k = ks[i];
+        uint16_t* out = outs[i];
+        int64_t running = 0;
+        for (int64_t t : p->sub_tensors[k]) {
+            zero3_status st = ZERO3_OK;
+            if (p->persistent[t]) {
+                st = L.add(persist_param, nullptr, p->offset[t], out + running, p->numel[t]);
+            } else {
+                for (int64_t s = p->seg_begin[t]; s < p->seg_begin[t + 1] && st == ZERO3_OK; ++s) {
+                    const zero3_segment& sg = p->segs[s];
+                    st = L.add(sparam[sg.rank], nullptr, sg.shard_off, out + running + sg.tensor_off,
+                               sg.len);
+                }
+            }
+            if (st != ZERO3_OK) return st;
+            running += p->numel[t];
+        }
+    }
+    zero3_status st = L.flush();
+    if (n_launches) *n_launches = L.launches();
+    return st;
 }
 
 }  // namespace z3
@@ -287,13 +384,22 @@ zero3_status zero3_allgather(const zero3_plan* p, const uint16_t* const* sparam,
     if (!p || !range_ok(p, lo, hi)) return ZERO3_EINVAL;
     if (lo == hi) return ZERO3_OK;
     if (!sparam || !full || !aligned16(full)) return ZERO3_EINVAL;
-    RankPtrs rp;
-    rp.full = full;
-    rp.in = reinterpret_cast<const void* const*>(sparam);
-    StreamArgs a;
-    zero3_status st = build_args(p, z3::kGather, rp, lo, hi, nullptr, 0, a);
-    if (st != ZERO3_OK) return st;
-    return cuda_status(z3::launch_stream(z3::kGather, a, stream));
+    for (int r = 0; r < p->n_ranks; ++r) {
+        int64_t la, lb;
+        rank_range(p, r, lo, hi, &la, &lb);
+        if (lb > la && (!sparam[r] || !aligned16(sparam[r]))) return ZERO3_EINVAL;
+    }
+    // one piece per owning rank: full[r*S + i] = sparam[r][i]
+    z3::PieceLauncher L(z3::kPieceBf16, stream, false);
+    for (int r = 0; r < p->n_ranks; ++r) {
+        int64_t la, lb;
+        rank_range(p, r, lo, hi, &la, &lb);
+        if (lb <= la) continue;
+        zero3_status st = L.add(sparam[r], nullptr, la, full + static_cast<int64_t>(r) * p->S + la,
+                                lb - la);
+        if (st != ZERO3_OK) return st;
+    }
+    return L.flush();
 }
 
 zero3_status zero3_step(const zero3_plan* p, const zero3_adamw_hparams* hp, int64_t t,
@@ -304,6 +410,11 @@ zero3_status zero3_step(const zero3_plan* p, const zero3_adamw_hparams* hp, int6
     if (!p || !range_ok(p, lo, hi) || !hparams_ok(hp, t) || grads_origin > lo)
         return ZERO3_EINVAL;
     const z3::Scalars sc = step_scalars(p, hp, t);
+    if (persist && !persist_ok(p, persist)) return ZERO3_EINVAL;
+    StreamArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.nd = p->n_ranks;
+    a.sc = sc;
     if (lo < hi) {
         if (!grads_ok(p, grads) || !sparam || !full || !aligned16(full)) return ZERO3_EINVAL;
         RankPtrs rp;
@@ -315,17 +426,12 @@ zero3_status zero3_step(const zero3_plan* p, const zero3_adamw_hparams* hp, int6
         rp.need_state = true;
         rp.out = reinterpret_cast<void* const*>(sparam);
         rp.full = full;
-        StreamArgs a;
         zero3_status st = build_args(p, z3::kFused, rp, lo, hi, &sc, 0, a);
         if (st != ZERO3_OK) return st;
-        // validate the persistent group before the first launch so that an
-        // error launches nothing
-        if (persist && !persist_ok(p, persist)) return ZERO3_EINVAL;
-        st = cuda_status(z3::launch_stream(z3::kFused, a, stream));
-        if (st != ZERO3_OK) return st;
     }
-    if (persist) return persistent_launch(p, sc, persist, stream);
-    return ZERO3_OK;
+    // the persistent group rides in the same launch as one more span
+    if (persist && p->psi_s > 0) add_persistent_span(p, persist, a);
+    return cuda_status(z3::launch_stream(z3::kFused, a, stream));
 }
 
 zero3_status zero3_step_stage12(const zero3_plan* p, const zero3_adamw_hparams* hp, int64_t t,
@@ -414,14 +520,24 @@ zero3_status zero3_allgather_qwz(const zero3_plan* p, int32_t bits, const int8_t
     if (bits != 8 && bits != 4) return ZERO3_EINVAL;
     if (lo == hi) return ZERO3_OK;
     if (!codes || !scales || !full || !aligned16(full)) return ZERO3_EINVAL;
-    RankPtrs rp;
-    rp.full = full;
-    rp.codes = const_cast<int8_t* const*>(codes);
-    rp.scales = const_cast<float* const*>(scales);
-    StreamArgs a;
-    zero3_status st = build_args(p, z3::kDequant, rp, lo, hi, nullptr, bits, a);
-    if (st != ZERO3_OK) return st;
-    return cuda_status(z3::launch_stream(z3::kDequant, a, stream));
+    for (int r = 0; r < p->n_ranks; ++r) {
+        int64_t la, lb;
+        rank_range(p, r, lo, hi, &la, &lb);
+        if (lb <= la) continue;
+        if (!codes[r] || !aligned16(codes[r]) || !scales[r] || !aligned16(scales[r]))
+            return ZERO3_EINVAL;
+    }
+    // one piece per owning rank: full[r*S + i] = bf16(code_r(i) * scale_r(i / 256))
+    z3::PieceLauncher L(bits == 4 ? z3::kPieceInt4 : z3::kPieceInt8, stream, false);
+    for (int r = 0; r < p->n_ranks; ++r) {
+        int64_t la, lb;
+        rank_range(p, r, lo, hi, &la, &lb);
+        if (lb <= la) continue;
+        zero3_status st = L.add(codes[r], scales[r], la,
+                                full + static_cast<int64_t>(r) * p->S + la, lb - la);
+        if (st != ZERO3_OK) return st;
+    }
+    return L.flush();
 }
 
 zero3_status zero3_persistent_step(const zero3_plan* p, const zero3_adamw_hparams* hp, int64_t t,
@@ -487,12 +603,68 @@ zero3_status zero3_fetch_submodule(zero3_plan* p, int32_t k, const uint16_t* con
             return ZERO3_ECUDA;
         }
     }
-    st = z3::gather_submodule(p, k, sparam, persist_param, out, stream);
+    uint16_t* outs[1] = {out};
+    st = z3::gather_submodules(p, &k, 1, sparam, persist_param, outs, stream);
     if (st != ZERO3_OK) return st;
     if (cudaEventRecord(p->events[k], stream) != cudaSuccess) return ZERO3_ECUDA;
     p->status[k] = ZERO3_INFLIGHT;
     p->refs[k] = 1;
     p->fetched_out[k] = out;
+    return ZERO3_OK;
+}
+
+zero3_status zero3_fetch_submodules(zero3_plan* p, const int32_t* ks, int32_t n,
+                                    const uint16_t* const* sparam, const uint16_t* persist_param,
+                                    uint16_t* const* outs, zero3_stream stream) {
+    if (!p || n < 0 || (n > 0 && (!ks || !outs))) return ZERO3_EINVAL;
+    const int32_t n_sub = static_cast<int32_t>(p->sub_tensors.size());
+    for (int32_t i = 0; i < n; ++i)
+        if (ks[i] < 0 || ks[i] >= n_sub) return ZERO3_EINVAL;
+    // Walk the list as n single fetches would, on the side: which
+    // submodules this call gathers, and the output each one is bound to.
+    std::vector<int32_t> gather;
+    std::vector<uint16_t*> gather_out;
+    std::vector<uint8_t> seen;       // gathered by this call
+    std::vector<uint16_t*> bound;    // ... into this output
+    try {
+        seen.assign(static_cast<size_t>(n_sub), 0);
+        bound.assign(static_cast<size_t>(n_sub), nullptr);
+        for (int32_t i = 0; i < n; ++i) {
+            const int32_t k = ks[i];
+            if (p->status[k] != ZERO3_NOT_AVAILABLE || seen[k]) {
+                // a later fetch adds a reference and must name the same out
+                const uint16_t* want = seen[k] ? bound[k] : p->fetched_out[k];
+                if (outs[i] != want) return ZERO3_ESTATE;
+                continue;
+            }
+            zero3_status st = z3::check_gather_sources(p, k, sparam, persist_param, outs[i]);
+            if (st != ZERO3_OK) return st;
+            seen[k] = 1;
+            bound[k] = outs[i];
+            gather.push_back(k);
+            gather_out.push_back(outs[i]);
+        }
+    } catch (const std::bad_alloc&) {
+        return ZERO3_ENOMEM;
+    }
+    for (int32_t k : gather) {
+        if (!p->events[k] &&
+            cudaEventCreateWithFlags(&p->events[k], cudaEventDisableTiming) != cudaSuccess) {
+            p->events[k] = nullptr;
+            return ZERO3_ECUDA;
+        }
+    }
+    zero3_status st = z3::gather_submodules(p, gather.data(), static_cast<int64_t>(gather.size()),
+                                            sparam, persist_param, gather_out.data(), stream);
+    if (st != ZERO3_OK) return st;
+    for (size_t j = 0; j < gather.size(); ++j) {
+        const int32_t k = gather[j];
+        if (cudaEventRecord(p->events[k], stream) != cudaSuccess) return ZERO3_ECUDA;
+        p->status[k] = ZERO3_INFLIGHT;
+        p->refs[k] = 0;
+        p->fetched_out[k] = gather_out[j];
+    }
+    for (int32_t i = 0; i < n; ++i) p->refs[ks[i]] += 1;
     return ZERO3_OK;
 }
 

@@ -196,8 +196,9 @@ zero3_status gather(zero3_coordinator* c, int32_t k, bool evict) {
             if (seq > 0 &&
                 cudaStreamWaitEvent(c->prefetch, c->rel[seq % kReleaseRing], 0) != cudaSuccess)
                 return ZERO3_ECUDA;
-            zero3_status st = z3::gather_submodule(c->plan, k, c->sparam.data(), c->persist,
-                                                   c->arena + o, c->prefetch);
+            uint16_t* outs[1] = {c->arena + o};
+            zero3_status st = z3::gather_submodules(c->plan, &k, 1, c->sparam.data(), c->persist,
+                                                    outs, c->prefetch);
             if (st != ZERO3_OK) return st;
             if (cudaEventRecord(c->ready[k], c->prefetch) != cudaSuccess) return ZERO3_ECUDA;
             c->off[k] = o;

@@ -5,9 +5,10 @@
 // the bf16 shard and the bf16 all-gather copy, with about 20 binary32
 // operations in between.  There is no contraction, so no tensor core work.
 //
-// Work layout.  A launch covers up to ZERO3_MAX_RANKS "spans"; a span is one
-// owner's slice [lo, hi) of local indices (a rank's shard, or the persistent
-// group).  The spans' elements are cut into chunks of 8 consecutive local
+// Work layout.  A launch covers up to ZERO3_MAX_RANKS + 1 "spans"; a span is
+// one owner's slice [lo, hi) of local indices (a rank's shard, or the
+// persistent group, which the fused step takes as one more span with its own
+// gradient buffers).  The spans' elements are cut into chunks of 8 consecutive local
 // indices aligned to multiples of 8, numbered consecutively across spans.
 // Thread c of the grid takes chunk c, so the 32 lanes of a warp
 // touch 32 adjacent chunks: 512 contiguous bytes of every bf16 stream and
@@ -36,7 +37,7 @@ namespace z3 {
 
 // Kernel parameters are passed by value; 32764 bytes is the limit.
 static_assert(sizeof(StreamArgs) <= 32764, "StreamArgs exceeds the kernel parameter limit");
-static_assert(sizeof(GatherArgs) <= 32764, "GatherArgs exceeds the kernel parameter limit");
+static_assert(sizeof(PieceArgs<kLargePieces>) <= 32764, "PieceArgs exceeds the kernel parameter limit");
 
 namespace {
 
@@ -221,22 +222,28 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 // rank).  `window`: the chunk's neighbours on both sides lie in the span, so
 // a phased chunk may be read as the two aligned 16-byte blocks around it.
 // All loads are issued before the first add.
+// Rank q's gradient buffer of a span: the flat chunk's (grads) or, for the
+// persistent group's span (pg), the persistent group's own (pgrads).
+__device__ __forceinline__ const uint16_t* grad_base(const StreamArgs& a, int q, bool pg) {
+    return pg ? a.pgrads[q] : a.grads[q];
+}
+
 template <int ND>
 __device__ __forceinline__ void reduce8(const StreamArgs& a, int64_t off, int ph, bool window,
-                                        float* g) {
+                                        bool pg, float* g) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) g[e] = 0.0f;
     if constexpr (ND > 0) {
         uint4 raw[ND];
         if (ph == 0) {
 #pragma unroll
-            for (int q = 0; q < ND; ++q) raw[q] = ldcs16(a.grads[q] + off);
+            for (int q = 0; q < ND; ++q) raw[q] = ldcs16(grad_base(a, q, pg) + off);
         } else if (window) {
 #pragma unroll
-            for (int q = 0; q < ND; ++q) raw[q] = ld8_window(a.grads[q] + off, ph);
+            for (int q = 0; q < ND; ++q) raw[q] = ld8_window(grad_base(a, q, pg) + off, ph);
         } else {
 #pragma unroll
-            for (int q = 0; q < ND; ++q) raw[q] = ld8_phase(a.grads[q] + off, ph);
+            for (int q = 0; q < ND; ++q) raw[q] = ld8_phase(grad_base(a, q, pg) + off, ph);
         }
 #pragma unroll
         for (int q = 0; q < ND; ++q) {
@@ -252,7 +259,7 @@ __device__ __forceinline__ void reduce8(const StreamArgs& a, int64_t off, int ph
             const int n = (nd - q0) < 8 ? (nd - q0) : 8;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-                if (k < n) raw[k] = ld8_phase(a.grads[q0 + k] + off, ph);
+                if (k < n) raw[k] = ld8_phase(grad_base(a, q0 + k, pg) + off, ph);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 if (k < n) {
@@ -269,10 +276,10 @@ __device__ __forceinline__ void reduce8(const StreamArgs& a, int64_t off, int ph
 }
 
 template <int ND>
-__device__ __forceinline__ float reduce1(const StreamArgs& a, int64_t off) {
+__device__ __forceinline__ float reduce1(const StreamArgs& a, int64_t off, bool pg) {
     float s = 0.0f;
     const int nd = ND > 0 ? ND : a.nd;
-    for (int q = 0; q < nd; ++q) s = __fadd_rn(s, bf16_f32(a.grads[q][off]));
+    for (int q = 0; q < nd; ++q) s = __fadd_rn(s, bf16_f32(grad_base(a, q, pg)[off]));
     return __fmul_rn(s, a.sc.inv_nd);
 }
 
@@ -283,7 +290,8 @@ __device__ __forceinline__ void vector_chunk(const StreamArgs& a, const Span& sp
     if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ || MODE == kReduce) {
         // blocks of a phased chunk: local [i0 - ph, i0 - ph + 16) within [i0 - 8, i0 + 16)
         const bool window = i0 - 8 >= sp.lo && i0 + 16 <= sp.hi;
-        reduce8<ND>(a, sp.gofs + i0, sp.gphase, window, g);
+        // only the fused step carries the persistent group's span
+        reduce8<ND>(a, sp.gofs + i0, sp.gphase, window, MODE == kFused && sp.pg != 0, g);
     }
     if constexpr (MODE == kQuant) {
         unpack8(ldcs16(static_cast<const uint16_t*>(sp.in) + i0), hq);
@@ -370,30 +378,14 @@ __device__ __forceinline__ void scalar_chunk(const StreamArgs& a, const Span& sp
             hq[e] = bf16_f32(static_cast<const uint16_t*>(sp.in)[i]);
             continue;
         }
-        if constexpr (MODE == kDequant) {
-            int c;
-            if constexpr (GT == 4) {
-                const uint32_t b = reinterpret_cast<const uint8_t*>(sp.codes)[i / 2];
-                c = static_cast<int>(b << (28 - 4 * (i & 1))) >> 28;  // sign-extend the nibble
-            } else {
-                c = sp.codes[i];
-            }
-            const float y = __fmul_rn(static_cast<float>(c), sp.scales[i / kQwzBlock]);
-            a.full[sp.fofs + i] = to_bf16(y);
-            continue;
-        }
         float g = 0.0f;
         if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ || MODE == kReduce)
-            g = reduce1<ND>(a, sp.gofs + i);
+            g = reduce1<ND>(a, sp.gofs + i, MODE == kFused && sp.pg != 0);
         if constexpr (MODE == kReduce) {
             if constexpr (GT == ZERO3_BF16)
                 static_cast<uint16_t*>(sp.out)[i] = to_bf16(g);
             else
                 static_cast<float*>(sp.out)[i] = g;
-            continue;
-        }
-        if constexpr (MODE == kGather) {
-            a.full[sp.fofs + i] = static_cast<const uint16_t*>(sp.in)[i];
             continue;
         }
         if constexpr (MODE == kAdam) {
@@ -471,233 +463,239 @@ __device__ __forceinline__ void qwz_block(const Span& sp, int64_t i0, const floa
     }
 }
 
-// Chunks per thread.  The copy-like modes move few bytes per chunk (2-3 B
-// per element); a thread then takes 4 chunks, block-interleaved so every
-// warp instruction stays contiguous: measured +9% (gather) and +22%
-// (dequantizing all-gather) at 1.3B, and a later sweep of 2 to 16 kept 4.
-// The fused modes keep one chunk per thread (more registers per chunk; 2 per
-// thread measured slightly slower).
-constexpr int kCopyChunks = 4;
-// The int4 dequantizing all-gather loads only 4 bytes of codes per chunk.
-constexpr int kCopyChunksInt4 = 4;
-// Submodule gather (zero3_fetch_submodule and the prefetch coordinator).
-constexpr int kFetchChunks = 4;
-
-template <int MODE, int GT>
-__host__ __device__ constexpr int chunks_per_thread() {
-    return MODE == kGather ? kCopyChunks
-           : MODE == kDequant ? (GT == 4 ? kCopyChunksInt4 : kCopyChunks)
-                              : 1;
-}
-
-// The copy-like modes (all-gather copy, dequantizing all-gather): every
-// chunk of the thread is loaded before any is stored.  The compiler cannot
-// hoist a load above a store through another pointer (they may alias), so a
-// load-store loop would keep one load in flight per thread.  Edge chunks of
-// a span take the element path in the first phase.
-template <int MODE, int GT, bool PHASED>
-__device__ __forceinline__ void copy_chunks(const StreamArgs& a, int64_t base, int& s) {
-    constexpr int CPT = chunks_per_thread<MODE, GT>();
-    uint4 raw[CPT];      // kGather: 8 bf16; kDequant: the codes (.x, and .y for int8)
-    float scl[CPT];      // kDequant: the block scale
-    uint16_t* dst[CPT];  // first element of the chunk in `full`, or null
-    int ph[CPT];
-    int sidx[CPT];       // span of the chunk
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-        dst[j] = nullptr;
-        if constexpr (PHASED) sidx[j] = -1;
-        const int64_t c = base + static_cast<int64_t>(j) * blockDim.x;
-        if (c >= a.total_chunks) continue;
-        while (s + 1 < a.n_spans && c >= a.span[s + 1].chunk0) ++s;
-        const Span& sp = a.span[s];
-        const int64_t i0 = (sp.lo & ~static_cast<int64_t>(7)) + ((c - sp.chunk0) << 3);
-        if (i0 >= sp.lo && i0 + 8 <= sp.hi) {
-            if constexpr (MODE == kGather) {
-                raw[j] = ldcs16(static_cast<const uint16_t*>(sp.in) + i0);
-            } else if constexpr (GT == 4) {
-                // 8 two's-complement nibbles, element i0+e in bits 4e..4e+3
-                raw[j].x = __ldcs(reinterpret_cast<const unsigned int*>(
-                    reinterpret_cast<const uint8_t*>(sp.codes) + i0 / 2));
-                scl[j] = sp.scales[i0 / kQwzBlock];
-            } else {
-                const uint2 q = __ldcs(reinterpret_cast<const uint2*>(sp.codes + i0));
-                raw[j].x = q.x;
-                raw[j].y = q.y;
-                scl[j] = sp.scales[i0 / kQwzBlock];
-            }
-            dst[j] = a.full + sp.fofs + i0;
-            ph[j] = sp.fphase;
-            if constexpr (PHASED) sidx[j] = s;
-        } else {
-            float unused[8];
-            scalar_chunk<MODE, 1, GT>(a, sp, i0, unused);
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-        // For a fixed j the warp's lanes hold consecutive chunks: a phased
-        // destination is stored by the whole warp when all 32 hold vector
-        // chunks of one span (warp-uniform decision, taken before any lane
-        // leaves the loop body).
-        bool warp_store = false;
-        if constexpr (PHASED) {
-            if (__activemask() == 0xffffffffu) {
-                const int s0 = __shfl_sync(0xffffffffu, sidx[j], 0);
-                warp_store = __all_sync(0xffffffffu,
-                                        dst[j] != nullptr && sidx[j] == s0 && ph[j] != 0);
-            }
-        }
-        if (!dst[j]) continue;
-        uint4 x;
-        if constexpr (MODE == kGather) {
-            x = raw[j];
-        } else {
-            float y[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                int c;
-                if constexpr (GT == 4) {
-                    c = static_cast<int>(raw[j].x << (28 - 4 * e)) >> 28;
-                } else {
-                    const uint32_t w = e < 4 ? raw[j].x : raw[j].y;
-                    c = static_cast<int8_t>((w >> (8 * (e & 3))) & 0xffu);
-                }
-                y[e] = __fmul_rn(static_cast<float>(c), scl[j]);
-            }
-            x = pack8(y);
-        }
-        if (warp_store)
-            st8_warp(dst[j], ph[j], x, warp_block(ph[j], x));
-        else
-            st8_phase(dst[j], ph[j], x);
-    }
-}
-
 // Resident blocks of 256 threads per SM that the register allocation must
 // allow.  The modes that reduce gradients with a compile-time rank count keep
 // 4 (at most 64 registers a thread): the ZeRO-1/2 step at N_d = 8 otherwise
-// takes 75 and the reduce-scatter 80, and both drop to 3 blocks.  The
-// dequantizing all-gather keeps 5 when aligned (at most 48 registers: 6094
-// against 5656 GB/s with 64) and 4 when phased (3571 against 3158 GB/s with
-// 72 at N_d = 7).  None of these spills.
-template <int MODE, int ND, bool PHASED>
+// takes 75 and the reduce-scatter 80, and both drop to 3 blocks.  None of
+// them spills.
+template <int MODE, int ND>
 __host__ __device__ constexpr int min_blocks_per_sm() {
     return (ND > 0 && (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ ||
-                       MODE == kReduce))                                         ? 4
-           : (MODE == kDequant && !PHASED)                                       ? 5
-           : (MODE == kDequant)                                                  ? 4
-                                                                                 : 1;
+                       MODE == kReduce))
+               ? 4
+               : 1;
 }
 
-// PHASED (copy modes only): some span's all-gather destination is not
-// 16-byte aligned, so the warp-cooperative store path is compiled in; the
-// aligned instantiation keeps fewer registers.
-template <int MODE, int ND, int GT, bool PHASED>
-__global__ void __launch_bounds__(kThreads, min_blocks_per_sm<MODE, ND, PHASED>())
+template <int MODE, int ND, int GT>
+__global__ void __launch_bounds__(kThreads, min_blocks_per_sm<MODE, ND>())
     stream_kernel(const __grid_constant__ StreamArgs a) {
     wait_prior_grids();
     allow_next_grid();
-    constexpr int CPT = chunks_per_thread<MODE, GT>();
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * CPT;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     int s = 0;
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * CPT + threadIdx.x;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
          base < a.total_chunks; base += stride) {
-        if constexpr (MODE == kGather || MODE == kDequant) {
-            copy_chunks<MODE, GT, PHASED>(a, base, s);
-        } else {
+        // one chunk per thread (the single-iteration loop keeps the code
+        // shape under which no instantiation spills)
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) {
-                const int64_t c = base + static_cast<int64_t>(j) * blockDim.x;
-                if (c >= a.total_chunks) break;
-                while (s + 1 < a.n_spans && c >= a.span[s + 1].chunk0) ++s;
-                const Span& sp = a.span[s];
-                const int64_t i0 = (sp.lo & ~static_cast<int64_t>(7)) + ((c - sp.chunk0) << 3);
-                float hq[8];
-                const bool vec = i0 >= sp.lo && i0 + 8 <= sp.hi;
-                // A phased all-gather stream is stored by the whole warp at
-                // once when its 32 lanes hold vector chunks of one span (a
-                // warp-uniform decision: every active lane takes part in it,
-                // and a partial or diverged warp keeps the per-lane stores).
-                bool warp_store = false;
-                if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ) {
-                    const unsigned active = __activemask();
-                    if (active == 0xffffffffu) {
-                        const int s0 = __shfl_sync(0xffffffffu, s, 0);
-                        warp_store = __all_sync(0xffffffffu, vec && s == s0 && sp.fofs >= 0 &&
-                                                                 sp.fphase != 0);
-                    }
+        for (int j = 0; j < 1; ++j) {
+            const int64_t c = base + static_cast<int64_t>(j) * blockDim.x;
+            if (c >= a.total_chunks) break;
+            while (s + 1 < a.n_spans && c >= a.span[s + 1].chunk0) ++s;
+            const Span& sp = a.span[s];
+            const int64_t i0 = (sp.lo & ~static_cast<int64_t>(7)) + ((c - sp.chunk0) << 3);
+            float hq[8];
+            const bool vec = i0 >= sp.lo && i0 + 8 <= sp.hi;
+            // A phased all-gather stream is stored by the whole warp at once
+            // when its 32 lanes hold vector chunks of one span (a
+            // warp-uniform decision: every active lane takes part in it, and
+            // a partial or diverged warp keeps the per-lane stores).
+            bool warp_store = false;
+            if constexpr (MODE == kFused || MODE == kFusedRep || MODE == kFusedQ) {
+                const unsigned active = __activemask();
+                if (active == 0xffffffffu) {
+                    const int s0 = __shfl_sync(0xffffffffu, s, 0);
+                    warp_store = __all_sync(0xffffffffu, vec && s == s0 && sp.fofs >= 0 &&
+                                                             sp.fphase != 0);
                 }
-                if (vec)
-                    vector_chunk<MODE, ND, GT>(a, sp, i0, hq, warp_store);
-                else
-                    scalar_chunk<MODE, ND, GT>(a, sp, i0, hq);
-                if constexpr (MODE == kFusedQ || MODE == kQuant)
-                    qwz_block<GT == 4 ? 4 : 8>(sp, i0, hq);
             }
+            if (vec)
+                vector_chunk<MODE, ND, GT>(a, sp, i0, hq, warp_store);
+            else
+                scalar_chunk<MODE, ND, GT>(a, sp, i0, hq);
+            if constexpr (MODE == kFusedQ || MODE == kQuant)
+                qwz_block<GT == 4 ? 4 : 8>(sp, i0, hq);
         }
     }
 }
 
-// A thread's kFetchChunks chunks are loaded before any of them is stored: the
-// compiler cannot move a load above a store to `out` (the pointers may
-// alias), so a load-store-load-store loop keeps one 16-byte load in flight
-// per thread.  Edge chunks of a piece (rare) are copied element by element
-// in the first phase.
-// PHASED: some piece's source is not 16-byte aligned relative to `out`.  The
-// aligned instantiation keeps fewer registers (one block per chunk) and so
-// more blocks per SM.
-template <bool PHASED>
-__global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherArgs a) {
+// ------------------------------------------------------------ piece kernel
+//
+// Copy-like work: submodule gathers (one or many submodules per launch), the
+// all-gather copy sparam -> full and the dequantizing qwZ all-gather.  Every
+// byte moves once, so the kernel is bound by HBM bandwidth with few
+// operations per byte; what matters is many independent 16-byte requests in
+// flight and no narrow or partial accesses.
+//
+// Chunks are aligned to the DESTINATION, so every store is one aligned
+// 16-byte store; a source at a nonzero phase is realigned on the way in.
+// A warp's 32 lanes hold 32 consecutive chunks of one piece (per step j of
+// the thread's four chunks), so lane l loads the aligned source unit under
+// its chunk and takes lane l+1's by shuffle (lane 31 loads the one after):
+// one aligned load per chunk.  Chunks whose source units would reach past
+// either end of the piece (at most two per piece edge) are copied element by
+// element.  Each lane issues all of its loads before its first store (the
+// compiler cannot move a load above a store through a possibly aliasing
+// pointer, which would leave one load in flight per lane).
+constexpr int kPieceChunks = kPieceWarpChunks / 32;   // chunks per lane
+
+// Source unit of a chunk and its realignment, per kind.
+//   bf16: 8 elements per aligned 16-byte unit; ph elements.
+//   int8: 8 codes per aligned 8-byte unit; ph bytes.
+//   int4: 8 codes per aligned 4-byte unit; ph nibbles.
+template <int KIND>
+struct Unit;
+template <>
+struct Unit<kPieceBf16> {
+    using T = uint4;
+    static __device__ __forceinline__ T load(const void* src, int64_t idx) {
+        return ldcs16(static_cast<const uint16_t*>(src) + idx);
+    }
+    static __device__ __forceinline__ T shfl(const T& x) {
+        T n;
+        n.x = __shfl_down_sync(0xffffffffu, x.x, 1);
+        n.y = __shfl_down_sync(0xffffffffu, x.y, 1);
+        n.z = __shfl_down_sync(0xffffffffu, x.z, 1);
+        n.w = __shfl_down_sync(0xffffffffu, x.w, 1);
+        return n;
+    }
+    static __device__ __forceinline__ T realign(const T& a, const T& b, int ph) {
+        return realign8(a, b, ph);
+    }
+};
+template <>
+struct Unit<kPieceInt8> {
+    using T = uint2;
+    static __device__ __forceinline__ T load(const void* src, int64_t idx) {
+        return __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(src) + idx));
+    }
+    static __device__ __forceinline__ T shfl(const T& x) {
+        return make_uint2(__shfl_down_sync(0xffffffffu, x.x, 1),
+                          __shfl_down_sync(0xffffffffu, x.y, 1));
+    }
+    // bytes ph..ph+7 of the 16 bytes a, b: words k..k+2 (k = ph / 4),
+    // funnel-shifted right by 8 * (ph % 4) bits
+    static __device__ __forceinline__ T realign(const T& a, const T& b, int ph) {
+        const bool k = (ph & 4) != 0;
+        const uint32_t sh = static_cast<uint32_t>(ph & 3) * 8u;
+        const uint32_t t0 = k ? a.y : a.x, t1 = k ? b.x : a.y, t2 = k ? b.y : b.x;
+        return make_uint2(__funnelshift_r(t0, t1, sh), __funnelshift_r(t1, t2, sh));
+    }
+};
+template <>
+struct Unit<kPieceInt4> {
+    using T = uint32_t;
+    static __device__ __forceinline__ T load(const void* src, int64_t idx) {
+        return __ldcs(static_cast<const unsigned int*>(src) + idx / 8);
+    }
+    static __device__ __forceinline__ T shfl(const T& x) {
+        return __shfl_down_sync(0xffffffffu, x, 1);
+    }
+    static __device__ __forceinline__ T realign(const T& a, const T& b, int ph) {
+        return __funnelshift_r(a, b, static_cast<uint32_t>(ph) * 4u);
+    }
+};
+
+// The 8 destination values of a chunk from its realigned source unit.
+// Dequantizing kinds: y = bf16_rne(f32(code) * scale), the scale of each
+// element's own 256-element block (a chunk may straddle two blocks).
+template <int KIND>
+__device__ __forceinline__ uint4 convert8(const typename Unit<KIND>::T& u, const Piece& P,
+                                          int64_t e0) {
+    if constexpr (KIND == kPieceBf16) {
+        return u;
+    } else {
+        const float sc0 = P.scales[e0 / kQwzBlock];
+        const float sc1 = P.scales[(e0 + 7) / kQwzBlock];
+        const int64_t edge = (e0 / kQwzBlock + 1) * kQwzBlock;  // first element of the next block
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            int c;
+            if constexpr (KIND == kPieceInt4) {
+                c = static_cast<int>(u << (28 - 4 * e)) >> 28;  // sign-extend nibble e
+            } else {
+                const uint32_t w = e < 4 ? u.x : u.y;
+                c = static_cast<int8_t>((w >> (8 * (e & 3))) & 0xffu);
+            }
+            y[e] = __fmul_rn(static_cast<float>(c), e0 + e < edge ? sc0 : sc1);
+        }
+        return pack8(y);
+    }
+}
+
+// Destination element d of piece P, element by element (chunks at the
+// piece's edges).
+template <int KIND>
+__device__ __forceinline__ uint16_t piece_element(const Piece& P, int64_t d) {
+    const int64_t e = P.s0 + d;
+    if constexpr (KIND == kPieceBf16) {
+        return static_cast<const uint16_t*>(P.src)[e];
+    } else {
+        int c;
+        if constexpr (KIND == kPieceInt4) {
+            const uint32_t b = static_cast<const uint8_t*>(P.src)[e / 2];
+            c = static_cast<int>(b << (28 - 4 * (e & 1))) >> 28;
+        } else {
+            c = static_cast<const int8_t*>(P.src)[e];
+        }
+        return to_bf16(__fmul_rn(static_cast<float>(c), P.scales[e / kQwzBlock]));
+    }
+}
+
+// PHASED: some piece of the launch has a nonzero source phase; the aligned
+// instantiation has no shuffles and fewer registers.
+template <int KIND, bool PHASED, int MAXP>
+__global__ void __launch_bounds__(kThreads, PHASED ? 4 : 5)
+    piece_kernel(const __grid_constant__ PieceArgs<MAXP> a) {
     wait_prior_grids();
     allow_next_grid();
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * kFetchChunks;
-    int s = 0;
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * kFetchChunks + threadIdx.x;
-         base < a.total_chunks; base += stride) {
-        // Phase 1 only issues loads: an aligned source chunk as one 16-byte
-        // block, a phased one as the two aligned blocks around it when both
-        // lie in the piece ([d0 - 8, d0 + 16)).  Realignment waits for the
-        // data, so it happens in phase 2 with the stores.
-        uint4 b0[kFetchChunks], b1[kFetchChunks];
-        int ph[kFetchChunks];   // nonzero: b0, b1 are the blocks around a phased chunk
-        int64_t dst[kFetchChunks];   // element index of a vector store, or -1
+    using U = Unit<KIND>;
+    const uint32_t w = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    if (w >= a.warp0[a.n]) return;  // whole warps leave together
+    // the piece of warp w: the last i with warp0[i] <= w (same for every lane)
+    int lo = 0, hi = a.n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.warp0[mid] <= w)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const Piece& P = a.piece[lo];
+    const int lane = threadIdx.x & 31;
+    const int ph = PHASED ? P.ph : 0;
+    const int64_t c0 = static_cast<int64_t>(w - a.warp0[lo]) * kPieceWarpChunks + lane;
+    typename U::T cur[kPieceChunks], nxt[kPieceChunks];
+    bool vec[kPieceChunks];
+    // Phase 1: loads (and the element path of edge chunks).
 #pragma unroll
-        for (int j = 0; j < kFetchChunks; ++j) {
-            dst[j] = -1;
-            ph[j] = 0;
-            const int64_t c = base + static_cast<int64_t>(j) * blockDim.x;
-            if (c >= a.total_chunks) continue;
-            while (s + 1 < a.n_segs && c >= a.seg[s + 1].chunk0) ++s;
-            const GatherSeg& g = a.seg[s];
-            const int64_t d0 = (g.dst_off & ~static_cast<int64_t>(7)) + ((c - g.chunk0) << 3);
-            const int64_t end = g.dst_off + g.len;
-            if (d0 >= g.dst_off && d0 + 8 <= end) {
-                const uint16_t* src = g.src + (d0 - g.dst_off);
-                if (!PHASED || g.sphase == 0) {
-                    b0[j] = ldcs16(src);
-                } else if (d0 - 8 >= g.dst_off && d0 + 16 <= end) {
-                    const uint16_t* al = src - g.sphase;
-                    b0[j] = __ldg(reinterpret_cast<const uint4*>(al));
-                    b1[j] = __ldg(reinterpret_cast<const uint4*>(al + 8));
-                    ph[j] = g.sphase;
-                } else {
-                    b0[j] = ld8_phase(src, g.sphase);
-                }
-                dst[j] = d0;
-            } else {
-                for (int e = 0; e < 8; ++e) {
-                    const int64_t d = d0 + e;
-                    if (d >= g.dst_off && d < end) a.out[d] = g.src[d - g.dst_off];
-                }
-            }
+    for (int j = 0; j < kPieceChunks; ++j) {
+        const int64_t d0 = (c0 + 32 * j) * 8;
+        // the source unit under the chunk starts at destination index b
+        const int64_t b = d0 - ph;
+        vec[j] = b >= P.lo && b + (ph ? 16 : 8) <= P.hi;
+        if (b >= P.lo && b + 8 <= P.hi) cur[j] = U::load(P.src, P.s0 + b);
+        if (PHASED && ph && lane == 31 && vec[j]) nxt[j] = U::load(P.src, P.s0 + b + 8);
+        if (!vec[j]) {
+            const int64_t e0 = d0 > P.lo ? d0 : P.lo;
+            const int64_t e1 = d0 + 8 < P.hi ? d0 + 8 : P.hi;
+            for (int64_t d = e0; d < e1; ++d) P.dst[d] = piece_element<KIND>(P, d);
         }
+    }
+    // Phase 2: realign (the neighbour's unit by shuffle) and store.  The
+    // shuffles are reached by every lane of the warp: j and ph are the same
+    // for all of them.
 #pragma unroll
-        for (int j = 0; j < kFetchChunks; ++j) {
-            if (dst[j] < 0) continue;
-            const uint4 x = (PHASED && ph[j]) ? realign8(b0[j], b1[j], ph[j]) : b0[j];
-            *reinterpret_cast<uint4*>(a.out + dst[j]) = x;
+    for (int j = 0; j < kPieceChunks; ++j) {
+        typename U::T u = cur[j];
+        if (PHASED && ph) {
+            const typename U::T n = U::shfl(cur[j]);
+            u = U::realign(cur[j], lane == 31 ? nxt[j] : n, ph);
         }
+        if (!vec[j]) continue;
+        const int64_t d0 = (c0 + 32 * j) * 8;
+        *reinterpret_cast<uint4*>(P.dst + d0) = convert8<KIND>(u, P, P.s0 + d0);
     }
 }
 
@@ -732,18 +730,33 @@ cudaError_t launch_programmatic(void (*kernel)(Args), int grid, const Args& a,
 
 template <int MODE, int ND, int GT>
 cudaError_t launch_one(const StreamArgs& a, cudaStream_t stream) {
-    const int grid = grid_for(a.total_chunks, chunks_per_thread<MODE, GT>());
+    const int grid = grid_for(a.total_chunks);
     if (grid <= 0) return cudaSuccess;
-    cudaError_t e;
-    if constexpr (MODE == kGather || MODE == kDequant) {
-        bool phased = false;
-        for (int i = 0; i < a.n_spans; ++i) phased = phased || a.span[i].fphase != 0;
-        e = phased ? launch_programmatic(stream_kernel<MODE, ND, GT, true>, grid, a, stream)
-                   : launch_programmatic(stream_kernel<MODE, ND, GT, false>, grid, a, stream);
-    } else {
-        e = launch_programmatic(stream_kernel<MODE, ND, GT, false>, grid, a, stream);
-    }
+    const cudaError_t e = launch_programmatic(stream_kernel<MODE, ND, GT>, grid, a, stream);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int KIND, int MAXP>
+cudaError_t launch_pieces(const PieceArgs<MAXP>& a, cudaStream_t stream) {
+    const uint32_t warps = a.warp0[a.n];
+    if (a.n <= 0 || warps == 0) return cudaSuccess;
+    const int grid = static_cast<int>((warps + kThreads / 32 - 1) / (kThreads / 32));
+    bool phased = false;
+    for (int i = 0; i < a.n; ++i) phased = phased || a.piece[i].ph != 0;
+    const cudaError_t e =
+        phased ? launch_programmatic(piece_kernel<KIND, true, MAXP>, grid, a, stream)
+               : launch_programmatic(piece_kernel<KIND, false, MAXP>, grid, a, stream);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int MAXP>
+cudaError_t launch_pieces_kind(int kind, const PieceArgs<MAXP>& a, cudaStream_t stream) {
+    switch (kind) {
+        case kPieceBf16: return launch_pieces<kPieceBf16>(a, stream);
+        case kPieceInt8: return launch_pieces<kPieceInt8>(a, stream);
+        case kPieceInt4: return launch_pieces<kPieceInt4>(a, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 template <int MODE, int GT>
@@ -774,29 +787,23 @@ cudaError_t launch_stream(int mode, const StreamArgs& a, cudaStream_t stream) {
         case kQuant:
             return a.dtype == 4 ? launch_one<kQuant, 1, 4>(a, stream)
                                 : launch_one<kQuant, 1, 8>(a, stream);
-        case kDequant:
-            return a.dtype == 4 ? launch_one<kDequant, 1, 4>(a, stream)
-                                : launch_one<kDequant, 1, 8>(a, stream);
         case kReduce:
             return a.dtype == ZERO3_BF16 ? launch_nd<kReduce, ZERO3_BF16>(a, stream)
                                          : launch_nd<kReduce, ZERO3_F32>(a, stream);
         case kAdam:
             return a.dtype == ZERO3_BF16 ? launch_one<kAdam, 1, ZERO3_BF16>(a, stream)
                                          : launch_one<kAdam, 1, ZERO3_F32>(a, stream);
-        case kGather: return launch_one<kGather, 1, 0>(a, stream);
         case kCast: return launch_one<kCast, 1, 0>(a, stream);
     }
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream) {
-    if (a.total_chunks <= 0) return cudaSuccess;
-    const int grid = grid_for(a.total_chunks, kFetchChunks);
-    bool phased = false;
-    for (int i = 0; i < a.n_segs; ++i) phased = phased || a.seg[i].sphase != 0;
-    const cudaError_t e = phased ? launch_programmatic(gather_kernel<true>, grid, a, stream)
-                                 : launch_programmatic(gather_kernel<false>, grid, a, stream);
-    return e != cudaSuccess ? e : cudaGetLastError();
+cudaError_t launch_pieces_small(int kind, const PieceArgs<kSmallPieces>& a, cudaStream_t stream) {
+    return launch_pieces_kind(kind, a, stream);
+}
+
+cudaError_t launch_pieces_large(int kind, const PieceArgs<kLargePieces>& a, cudaStream_t stream) {
+    return launch_pieces_kind(kind, a, stream);
 }
 
 }  // namespace z3

@@ -13,6 +13,9 @@ Layout (all separate allocations, each 512-byte aligned by the allocator):
   full          bf16  the flat all-gathered parameter buffer (psi_pad)
   pmaster/pm/pv fp32, pparam bf16: the one resident copy of the persistent group
   out           bf16  the submodule gather buffer (largest submodule)
+  arena         bf16  the gather buffers of one all-gather bucket (allocated on
+                      first use): each submodule of the bucket at its own
+                      16-byte aligned offset
 """
 from __future__ import annotations
 
@@ -85,6 +88,8 @@ class Emulation:
         self.pparam = A(self.psi_s, bf)
         self.max_sub = max([self.plan.submodule(k)[1] for k in range(info.n_submodules)] + [0])
         self.out = A(max(self.max_sub, 1), bf)
+        self.arena: Optional[torch.Tensor] = None
+        self._buckets: dict = {}
         self.persist = zero3.persist_state([_ptr(g) for g in self.pgrads], _ptr(self.pmaster),
                                            _ptr(self.pm), _ptr(self.pv), _ptr(self.pparam))
 
@@ -185,10 +190,64 @@ class Emulation:
     def release(self, k: int) -> None:
         zero3.zero3_release_submodule(self.plan, k)
 
-    def forward_backward_gathers(self) -> None:
+    def gather_buckets(self, bucket: int) -> List[List[int]]:
+        """Consecutive submodules grouped into buckets of at most `bucket`
+        elements (a larger submodule forms a bucket of its own)."""
+        if bucket in self._buckets:
+            return self._buckets[bucket]
+        groups: List[List[int]] = []
+        cur: List[int] = []
+        size = 0
+        for k in range(self.plan.info.n_submodules):
+            n = self.plan.submodule(k)[1]
+            if cur and size + n > bucket:
+                groups.append(cur)
+                cur, size = [], 0
+            cur.append(k)
+            size += n
+        if cur:
+            groups.append(cur)
+        self._buckets[bucket] = groups
+        return groups
+
+    def bucket_outputs(self, ks: Sequence[int]) -> List[int]:
+        """Device pointers of the gather buffers of submodules ks, each at a
+        16-byte aligned offset of the arena (grown to the largest bucket)."""
+        sizes = [(self.plan.submodule(k)[1] + 7) // 8 * 8 for k in ks]
+        need = max(sum(sizes), 8)
+        if self.arena is None or self.arena.numel() < need:
+            self.arena = self.alloc(need, torch.bfloat16)
+        base = self.arena.data_ptr()
+        outs, off = [], 0
+        for n in sizes:
+            outs.append(base + 2 * off)
+            off += n
+        return outs
+
+    def fetch_many(self, ks: Sequence[int]) -> List[int]:
+        """One zero3_fetch_submodules call for submodules ks; returns their
+        gather buffers."""
+        outs = self.bucket_outputs(ks)
+        zero3.zero3_fetch_submodules(self.plan, list(ks), self.ptrs(self.sparam),
+                                     _ptr(self.pparam), outs, self.sid)
+        return outs
+
+    def forward_backward_gathers(self, bucket: int = 0) -> None:
         """Gather every submodule before its forward (list order) and again
-        before its backward (reverse order), releasing after each use."""
+        before its backward (reverse order), releasing after each use.  With
+        bucket > 0 consecutive submodules of up to `bucket` elements are
+        gathered together (one zero3_fetch_submodules call per bucket),
+        forward in list order and backward in reverse."""
         n = self.plan.info.n_submodules
+        if bucket > 0:
+            groups = self.gather_buckets(bucket)
+            self.bucket_outputs(max(groups, key=lambda g: sum(
+                (self.plan.submodule(k)[1] + 7) // 8 * 8 for k in g)) if groups else [])
+            for ks in groups + [list(reversed(g)) for g in reversed(groups)]:
+                self.fetch_many(ks)
+                for k in ks:
+                    self.release(k)
+            return
         for k in range(n):
             self.fetch(k)
             self.release(k)

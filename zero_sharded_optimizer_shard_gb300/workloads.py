@@ -8,7 +8,8 @@ library, the tests and the benchmark.
 Hyper-parameters follow the AdamW block of the example DeepSpeed config in
 the ZERO tutorial (cnhsyj.com/news/20093, section 3.1 "基礎配置與啟動"):
 lr 5e-5, betas (0.9, 0.999), eps 1e-8, weight_decay 0.01, held constant.
-The persistence threshold 1e5 and bucket size 5e8 are the defaults quoted in
+The persistence threshold 1e5 and the reduce and all-gather bucket sizes
+5e8 are the defaults quoted in
 "DeepSpeed Zero-3 的参数分区与按需访问机制" (hotelren.com/news/4329759) and in
 its minimal ZeRO-3 config.
 """
@@ -20,6 +21,9 @@ from typing import List, Optional
 
 PERSISTENCE_THRESHOLD = 100_000
 REDUCE_BUCKET_SIZE = 500_000_000
+# parameter gathers are grouped into buckets of this many elements
+# (allgather_bucket_size of the same minimal config)
+ALLGATHER_BUCKET_SIZE = 500_000_000
 
 ADAMW = dict(lr=5e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
 
@@ -46,6 +50,7 @@ class Workload:
     outlier_sigma: float = 1e-1
     threshold: int = PERSISTENCE_THRESHOLD
     bucket: int = REDUCE_BUCKET_SIZE
+    gather_bucket: int = ALLGATHER_BUCKET_SIZE
     hparams: dict = field(default_factory=lambda: dict(ADAMW))
     names: Optional[List[str]] = None
     # rank-0 view: only ranks in `ranks` hold optimizer state on this device

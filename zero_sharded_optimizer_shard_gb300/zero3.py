@@ -113,6 +113,8 @@ _SIGS = [
     ("zero3_cast_params", C.c_int, [_vp, C.POINTER(_vp), C.POINTER(_vp), _vp,
                                     C.POINTER(PersistState), C.c_int64, C.c_int64, _vp]),
     ("zero3_fetch_submodule", C.c_int, [_vp, C.c_int32, C.POINTER(_vp), _vp, _vp, _vp]),
+    ("zero3_fetch_submodules", C.c_int, [_vp, _c_i32_p, C.c_int32, C.POINTER(_vp), _vp,
+                                         C.POINTER(_vp), _vp]),
     ("zero3_release_submodule", C.c_int, [_vp, C.c_int32]),
     ("zero3_submodule_status", C.c_int, [_vp, C.c_int32, _c_i32_p]),
     ("zero3_submodule_wait", C.c_int, [_vp, C.c_int32]),
@@ -310,6 +312,13 @@ def zero3_cast_params(plan: Plan, master, sparam, full, persist, flat_lo, flat_h
 def zero3_fetch_submodule(plan: Plan, k, sparam, persist_param, out, stream=0):
     _check(plan._lib.zero3_fetch_submodule(plan.handle, k, _ptrs(sparam), persist_param or None,
                                            out or None, stream), "zero3_fetch_submodule")
+
+
+def zero3_fetch_submodules(plan: Plan, ks, sparam, persist_param, outs, stream=0):
+    ka = (C.c_int32 * max(len(ks), 1))(*ks)
+    _check(plan._lib.zero3_fetch_submodules(plan.handle, ka, len(ks), _ptrs(sparam),
+                                            persist_param or None, _ptrs(outs), stream),
+           "zero3_fetch_submodules")
 
 
 def zero3_release_submodule(plan: Plan, k):

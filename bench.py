@@ -88,6 +88,9 @@ def parse(argv=None):
                     help="ablation: reduce-scatter (fp32 shard gradient), AdamW and all-gather "
                          "as three launches, each timed")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-copy-streams", type=int, choices=[1, 2], default=2,
+                    help="host copies of the end-to-end run on one stream (uploads and "
+                         "read-backs in turn) or two (concurrent)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=8.0,
                     help="seconds of oracle work per CPU-baseline measurement")
@@ -585,16 +588,23 @@ def run_coordinator(args):
         if backward:
             torch.matmul(Y[:, :cols], Wv.t(), out=dX)
 
+    host = {"s": 0.0, "n": 0}
+
     def one_step(co, t):
         for i, k in enumerate(trace):
             if co is None:
                 with torch.cuda.stream(compute):
                     gemms(Wfix, 0, k, i >= n_sub)
                 continue
+            h0 = time.perf_counter()
             ptr = co.fetch(k)
+            host["s"] += time.perf_counter() - h0
             with torch.cuda.stream(compute):
                 gemms(arena, (ptr - arena.data_ptr()) // 2, k, i >= n_sub)
+            h0 = time.perf_counter()
             co.release(k)
+            host["s"] += time.perf_counter() - h0
+            host["n"] += 1
         e.step(t)
         if co is not None:
             co.next_step()
@@ -614,13 +624,20 @@ def run_coordinator(args):
             one_step(co, t)
         torch.cuda.synchronize()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        host["s"], host["n"] = 0.0, 0
+        w0 = time.perf_counter()
         s0.record(compute)
         for _ in range(args.steps):
             t += 1
             one_step(co, t)
         s1.record(compute)
+        w1 = time.perf_counter()
         torch.cuda.synchronize()
-        results[mode] = {"ms_per_step": s0.elapsed_time(s1) / args.steps}
+        results[mode] = {"ms_per_step": s0.elapsed_time(s1) / args.steps,
+                         "host_ms_per_step_enqueue": (w1 - w0) * 1e3 / args.steps}
+        if host["n"]:
+            # host time of one coordinator fetch + release, through the binding
+            results[mode]["host_us_per_fetch"] = host["s"] / host["n"] * 1e6
         if co is not None:
             results[mode]["stats"] = co.stats()
         del co
@@ -966,35 +983,34 @@ def run_e2e(e, w, args, stream, n_params, t0):
     steps = max(2, min(args.steps, 6))
     lo = min(e.state_ranks) * e.S
     hi = min((max(e.state_ranks) + 1) * e.S, e.psi_pad)
-    need = sum(x.numel() * 2 for G in e.grads for x in G) + e.full.numel() * 2
+    # every rank's gradient buffer per chunk (the first also holds the
+    # persistent group's gradients after the flat ones)
+    need = sum(x.numel() * 2 for G in e.gbufs for x in G) + e.full.numel() * 2
     free, _ = torch.cuda.mem_get_info()
     if need > free - (2 << 30):
         return {"value": None, "unit": "params/s",
                 "note": f"second device buffer set ({need / 1e9:.0f} GB) does not fit"}
     try:
-        host_g = [[torch.empty(x.numel(), dtype=x.dtype, pin_memory=True) for x in G] for G in e.grads]
-        host_pg = [torch.empty(x.numel(), dtype=x.dtype, pin_memory=True) for x in e.pgrads]
+        host_g = [[torch.empty(x.numel(), dtype=x.dtype, pin_memory=True) for x in G]
+                  for G in e.gbufs]
         host_full = torch.empty(hi - lo, dtype=e.full.dtype, pin_memory=True)
-        dev_g = [e.grads, [[torch.empty_like(x) for x in G] for G in e.grads]]
-        dev_pg = [e.pgrads, [torch.empty_like(x) for x in e.pgrads]]
+        dev_g = [e.gbufs, [[torch.empty_like(x) for x in G] for G in e.gbufs]]
         dev_full = [e.full, torch.empty_like(e.full)]
     except RuntimeError as exc:
         return {"value": None, "unit": "params/s", "error": f"allocation failed: {exc}"}
-    for hG, G in zip(host_g, e.grads):
+    for hG, G in zip(host_g, e.gbufs):
         for h, d in zip(hG, G):
             h.copy_(d)
-    for h, d in zip(host_pg, e.pgrads):
-        h.copy_(d)
-    h2d = sum(x.numel() * 2 for hG in host_g for x in hG) + sum(x.numel() * 2 for x in host_pg)
+    h2d = sum(x.numel() * 2 for hG in host_g for x in hG)
     d2h = host_full.numel() * 2
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    # byte offset of the persistent group's gradients in each rank's first buffer
+    poff = e.pgrads[0].data_ptr() - e.gbufs[0][0].data_ptr() if e.gbufs else 0
 
     def upload(b):
         for hG, G in zip(host_g, dev_g[b]):
             for h, d in zip(hG, G):
                 d.copy_(h, non_blocking=True)
-        for h, d in zip(host_pg, dev_pg[b]):
-            d.copy_(h, non_blocking=True)
 
     # the host link alone: the same uploads and read-back, nothing else running
     link = {}
@@ -1018,37 +1034,46 @@ def run_e2e(e, w, args, stream, n_params, t0):
             for _ in range(steps)]
     computed = [ev() for _ in range(steps)]
     read = [ev() for _ in range(steps)]
+    # one copy stream: every copy in issue order (upload k+1, then read-back
+    # k); two: read-backs on their own stream, concurrent with uploads
+    down_s = up if args.e2e_copy_streams == 1 else down
+
+    def enqueue_upload(k):
+        with torch.cuda.stream(up):
+            if k >= 2:
+                up.wait_event(computed[k - 2])  # buffer set k % 2 was read by step k-2
+            up_t[k][0].record(up)
+            upload(k % 2)
+            up_t[k][1].record(up)
+            uploaded[k].record(up)
+
     torch.cuda.synchronize()
     t = t0
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.perf_counter()
     start.record(up)
+    enqueue_upload(0)
     for k in range(steps):
         b = k % 2
-        with torch.cuda.stream(up):
-            if k >= 2:
-                up.wait_event(computed[k - 2])  # buffer set b was read by step k-2
-            up_t[k][0].record(up)
-            upload(b)
-            up_t[k][1].record(up)
-            uploaded[k].record(up)
         stream.wait_event(uploaded[k])
         if k >= 2:
             stream.wait_event(read[k - 2])      # full[b] of step k-2 was read back
         t += 1
         e.forward_backward_gathers(bucket=w.gather_bucket)
-        ps = zero3.persist_state([x.data_ptr() for x in dev_pg[b]], e.pmaster.data_ptr(),
+        ps = zero3.persist_state([x.data_ptr() + poff for x in dev_g[b][0]], e.pmaster.data_ptr(),
                                  e.pm.data_ptr(), e.pv.data_ptr(), e.pparam.data_ptr())
         for c, ((clo, chi), G) in enumerate(zip(e.chunks, dev_g[b])):
             zero3.zero3_step(e.plan, e.hp, t, e.ptrs(G), clo, e.ptrs(e.master), e.ptrs(e.m),
                              e.ptrs(e.v), e.ptrs(e.sparam), dev_full[b].data_ptr(),
                              ps if c == 0 else None, clo, chi, e.sid)
         computed[k].record(stream)
-        with torch.cuda.stream(down):
-            down.wait_event(computed[k])
+        if k + 1 < steps:
+            enqueue_upload(k + 1)               # overlaps step k
+        with torch.cuda.stream(down_s):
+            down_s.wait_event(computed[k])
             host_full.copy_(dev_full[b][lo:hi], non_blocking=True)
-            read[k].record(down)
-    end.record(down)
+            read[k].record(down_s)
+    end.record(down_s)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     ms = start.elapsed_time(end) / steps
@@ -1064,7 +1089,11 @@ def run_e2e(e, w, args, stream, n_params, t0):
             "bound_ms_per_step": max(h2d / link["h2d"], d2h / link["d2h"]) / 1e6,
             "link_note": "host link measured in the same run: the same pinned buffers copied "
                          "alone, one copy per buffer, best of 2",
-            "pipeline": "uploads of step k+1 and read-back of step k overlap step k"}
+            "copy_streams": args.e2e_copy_streams,
+            "pipeline": ("upload of step k+1 overlaps step k; read-back of step k follows it on "
+                         "the same copy stream" if args.e2e_copy_streams == 1 else
+                         "upload of step k+1 and read-back of step k overlap step k, on two "
+                         "copy streams")}
 
 
 def main():

@@ -220,7 +220,12 @@ zero3_status zero3_allgather(const zero3_plan* plan, const uint16_t* const* spar
  * Results equal zero3_reduce_scatter(F32) + zero3_adamw_step(F32) +
  * zero3_allgather bit for bit.  If persist is not NULL the persistent group is
  * also updated (same arithmetic, DDP style, on its single resident copy),
- * whatever the range, in the same kernel launch: one launch per call. */
+ * whatever the range.  When every rank's persist->grads[q] lies at one common
+ * element offset from grads[q] (e.g. each rank's gradient buffer holds the
+ * flat gradients followed by the persistent group's, as one buffer of
+ * psi_pad + psi_s elements), the group is one more span of the same kernel
+ * launch and may have any element alignment; otherwise it is a second
+ * launch and its gradient pointers must be 16-byte aligned. */
 zero3_status zero3_step(const zero3_plan* plan, const zero3_adamw_hparams* hp, int64_t t,
                         const uint16_t* const* grads, int64_t grads_origin,
                         float* const* master, float* const* m, float* const* v,
@@ -383,7 +388,12 @@ zero3_status zero3_submodule_wait(zero3_plan* plan, int32_t k);
  *    gather; their contents change only through the optimizer step, after
  *    which the caller calls zero3_coordinator_next_step.
  *  - compute_stream and prefetch_stream must differ; the coordinator records
- *    events on both and never synchronises the host. */
+ *    events on both and never synchronises the host.
+ *  - Prefetches go out in batches: all submodules that fit the budgets at a
+ *    fetch are gathered by one zero3_fetch_submodules-style call (a few
+ *    launches of up to 512 pieces), with one wait for the arena ranges they
+ *    reuse; the compute stream waits on a ready event only if it has not
+ *    already waited on a later one of the prefetch stream. */
 typedef struct zero3_coordinator zero3_coordinator;
 
 typedef struct zero3_prefetch_config {
@@ -403,6 +413,9 @@ typedef struct zero3_coordinator_stats {
     int64_t gathered_elems;
     int64_t peak_live_elems;
     int64_t live_elems;
+    int64_t gather_calls;    /* batches issued (each gathers one or more submodules) */
+    int64_t gather_launches; /* kernel launches of those batches */
+    int64_t compute_waits;   /* waits of the compute stream on a ready event */
 } zero3_coordinator_stats;
 
 /* EINVAL: NULL plan/cfg/out, negative sizes, equal streams, arena smaller

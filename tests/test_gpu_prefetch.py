@@ -161,3 +161,23 @@ def test_odd_sized_submodules_share_the_arena():
     plan, before = oracle_params_by_step(w, 2)
     check(seen, plan, before)
     assert co.stats()["prefetch_hits"] > 0
+
+
+def test_prefetch_batches_many_small_submodules():
+    """Ragged list, arena for the whole model: the prefetch window goes out
+    as a few batched gathers (far fewer launches than submodules gathered),
+    the compute stream waits once per batch, and every copy still equals the
+    oracle's gather of the parameters before that step."""
+    w = W.ragged_small(7)
+    plan0 = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    total = sum(plan0.submodule_numel(k) for k in plan0.submodules)
+    big = max(plan0.submodule_numel(k) for k in plan0.submodules)
+    e, co, seen = run(w, 2, lambda t, n: fwd_bwd(n), arena_mult=2.2 * total / big, delay=False)
+    plan, before = oracle_params_by_step(w, 2)
+    check(seen, plan, before)
+    s = co.stats()
+    assert s["trace_misses"] == 0 and s["prefetched"] > 0
+    assert s["gather_launches"] * 10 < s["gathers"], s
+    assert s["gather_calls"] * 10 < s["gathers"], s
+    fetches = 2 * 2 * plan.n_submodules
+    assert s["compute_waits"] * 10 < fetches, s

@@ -142,24 +142,43 @@ bool persist_ok(const zero3_plan* p, const zero3_persist_state* ps) {
            aligned16(ps->master) && aligned16(ps->m) && aligned16(ps->v) && aligned16(ps->param);
 }
 
-// Appends the persistent group to a fused launch as one more span: local
-// indices [0, psi_s) of its resident copy, gradients from the group's own
-// per-rank buffers (pgrads), no write to `full`.  The arithmetic per element
-// is the flat spans' (fixed-order sum times 1/N_d, AdamW, bf16 cast).
-void add_persistent_span(const zero3_plan* p, const zero3_persist_state* ps, StreamArgs& a) {
-    for (int q = 0; q < p->n_ranks; ++q) a.pgrads[q] = ps->grads[q];
+// The persistent group as one span of a fused launch: local indices
+// [0, psi_s) of its resident copy, no write to `full`, gradients at element
+// offset gofs from the launch's gradient pointers (the arithmetic per element
+// is the flat spans').
+void add_persistent_span(const zero3_plan* p, const zero3_persist_state* ps, int64_t gofs,
+                         StreamArgs& a) {
     Span s;
     std::memset(&s, 0, sizeof(s));
     s.lo = 0;
     s.hi = p->psi_s;
-    s.gofs = 0;
+    s.gofs = gofs;
+    s.gphase = static_cast<int32_t>(gofs & 7);  // two's complement: also for gofs < 0
     s.fofs = -1;
-    s.pg = 1;
     s.master = ps->master;
     s.m = ps->m;
     s.v = ps->v;
     s.out = ps->param;
     add_span(a, s);
+}
+
+// When every rank's persistent-group gradient sits at the same element
+// offset from that rank's flat gradient pointer (for instance right after the
+// flat gradients in one buffer per rank), returns true and the offset: the
+// group can then ride in the flat launch as one more span.
+bool common_persist_offset(const zero3_plan* p, const uint16_t* const* grads,
+                           const zero3_persist_state* ps, int64_t* gofs) {
+    if (!grads || !ps || !ps->grads) return false;
+    int64_t d0 = 0;
+    for (int q = 0; q < p->n_ranks; ++q) {
+        if (!grads[q] || !ps->grads[q]) return false;
+        const int64_t d = static_cast<int64_t>(reinterpret_cast<uintptr_t>(ps->grads[q]) -
+                                               reinterpret_cast<uintptr_t>(grads[q]));
+        if (d % 2 != 0 || (q > 0 && d != d0)) return false;
+        d0 = d;
+    }
+    *gofs = d0 / 2;
+    return true;
 }
 
 zero3_status persistent_launch(const zero3_plan* p, const z3::Scalars& sc,
@@ -170,7 +189,8 @@ zero3_status persistent_launch(const zero3_plan* p, const z3::Scalars& sc,
     std::memset(&a, 0, sizeof(a));
     a.nd = p->n_ranks;
     a.sc = sc;
-    add_persistent_span(p, ps, a);
+    for (int q = 0; q < p->n_ranks; ++q) a.grads[q] = ps->grads[q];
+    add_persistent_span(p, ps, 0, a);
     return cuda_status(z3::launch_stream(z3::kFused, a, stream));
 }
 
@@ -198,15 +218,14 @@ zero3_status check_gather_sources(const zero3_plan* p, int32_t k, const uint16_t
 
 PieceLauncher::PieceLauncher(int kind, cudaStream_t stream, bool large)
     : kind_(kind), stream_(stream), large_(large) {
-    if (large)
-        args_ = new (std::nothrow) PieceArgs<kLargePieces>;
-    else
-        args_ = new (std::nothrow) PieceArgs<kSmallPieces>;
-    if (args_) {
-        if (large)
-            static_cast<PieceArgs<kLargePieces>*>(args_)->n = 0;
-        else
-            static_cast<PieceArgs<kSmallPieces>*>(args_)->n = 0;
+    if (large) {
+        auto* a = new (std::nothrow) PieceArgs<kLargePieces>;
+        if (a) a->n = 0;
+        args_ = a;
+    } else {
+        auto* a = new (std::nothrow) PieceArgs<kSmallPieces>;
+        if (a) a->n = 0;
+        args_ = a;
     }
 }
 
@@ -410,11 +429,18 @@ zero3_status zero3_step(const zero3_plan* p, const zero3_adamw_hparams* hp, int6
     if (!p || !range_ok(p, lo, hi) || !hparams_ok(hp, t) || grads_origin > lo)
         return ZERO3_EINVAL;
     const z3::Scalars sc = step_scalars(p, hp, t);
-    if (persist && !persist_ok(p, persist)) return ZERO3_EINVAL;
-    StreamArgs a;
-    std::memset(&a, 0, sizeof(a));
-    a.nd = p->n_ranks;
-    a.sc = sc;
+    const bool with_persist = persist && p->psi_s > 0;
+    int64_t pofs = 0;
+    const bool fold = with_persist && lo < hi && common_persist_offset(p, grads, persist, &pofs);
+    // validate the persistent group before the first launch so that an
+    // error launches nothing
+    if (with_persist) {
+        if (!persist->master || !persist->m || !persist->v || !persist->param ||
+            !aligned16(persist->master) || !aligned16(persist->m) || !aligned16(persist->v) ||
+            !aligned16(persist->param))
+            return ZERO3_EINVAL;
+        if (!fold && !persist_ok(p, persist)) return ZERO3_EINVAL;
+    }
     if (lo < hi) {
         if (!grads_ok(p, grads) || !sparam || !full || !aligned16(full)) return ZERO3_EINVAL;
         RankPtrs rp;
@@ -426,12 +452,16 @@ zero3_status zero3_step(const zero3_plan* p, const zero3_adamw_hparams* hp, int6
         rp.need_state = true;
         rp.out = reinterpret_cast<void* const*>(sparam);
         rp.full = full;
+        StreamArgs a;
         zero3_status st = build_args(p, z3::kFused, rp, lo, hi, &sc, 0, a);
         if (st != ZERO3_OK) return st;
+        // the persistent group rides in the same launch as one more span
+        if (fold) add_persistent_span(p, persist, pofs, a);
+        st = cuda_status(z3::launch_stream(z3::kFused, a, stream));
+        if (st != ZERO3_OK || fold) return st;
     }
-    // the persistent group rides in the same launch as one more span
-    if (persist && p->psi_s > 0) add_persistent_span(p, persist, a);
-    return cuda_status(z3::launch_stream(z3::kFused, a, stream));
+    if (with_persist) return persistent_launch(p, sc, persist, stream);
+    return ZERO3_OK;
 }
 
 zero3_status zero3_step_stage12(const zero3_plan* p, const zero3_adamw_hparams* hp, int64_t t,

@@ -28,6 +28,15 @@
 //  * At a step boundary (after the optimizer step was enqueued on the compute
 //    stream) every gathered copy is stale: all are dropped, and the prefetch
 //    stream waits for the optimizer step before gathering again.
+//  * Prefetches are issued as batches: every submodule that fits the budgets
+//    is placed in the arena first, the prefetch stream waits once for the
+//    latest release among their ranges, and one zero3_fetch_submodules-style
+//    gather (a few launches of up to 512 pieces) fills them all ("allgather
+//    bucket": many small gathers aggregated into few large ones, ZERO
+//    tutorial, cnhsyj.com, section 3.1).  Each submodule's ready event is
+//    recorded after the batch; events on the prefetch stream complete in
+//    order, so the compute stream waits on a ready event only if it has not
+//    already waited on a later one.
 #include <algorithm>
 #include <new>
 #include <vector>
@@ -69,6 +78,9 @@ struct zero3_coordinator {
     std::vector<int64_t> off;        // arena offset of a live submodule, -1 otherwise
     std::vector<uint8_t> ahead;      // gathered ahead of use and not fetched yet
     std::vector<cudaEvent_t> ready;
+    std::vector<uint64_t> ready_seq;  // position of ready[k] on the prefetch stream
+    uint64_t prefetch_seq = 0;        // events recorded on the prefetch stream so far
+    uint64_t compute_waited = 0;      // latest prefetch position the compute stream waited on
     int64_t live = 0, ahead_elems = 0;
 
     std::vector<FreeRange> free_list;
@@ -184,6 +196,7 @@ zero3_status gather(zero3_coordinator* c, int32_t k, bool evict) {
     const int64_t n = numel_of(c, k);
     if (n == 0) {  // nothing to gather: an empty view at the arena's start
         if (cudaEventRecord(c->ready[k], c->prefetch) != cudaSuccess) return ZERO3_ECUDA;
+        c->ready_seq[k] = ++c->prefetch_seq;
         c->off[k] = 0;
         c->status[k] = ZERO3_INFLIGHT;
         return ZERO3_OK;
@@ -197,14 +210,18 @@ zero3_status gather(zero3_coordinator* c, int32_t k, bool evict) {
                 cudaStreamWaitEvent(c->prefetch, c->rel[seq % kReleaseRing], 0) != cudaSuccess)
                 return ZERO3_ECUDA;
             uint16_t* outs[1] = {c->arena + o};
+            int64_t launches = 0;
             zero3_status st = z3::gather_submodules(c->plan, &k, 1, c->sparam.data(), c->persist,
-                                                    outs, c->prefetch);
+                                                    outs, c->prefetch, &launches);
             if (st != ZERO3_OK) return st;
             if (cudaEventRecord(c->ready[k], c->prefetch) != cudaSuccess) return ZERO3_ECUDA;
+            c->ready_seq[k] = ++c->prefetch_seq;
             c->off[k] = o;
             c->live += n;
             c->status[k] = ZERO3_INFLIGHT;
             c->stats.gathers += 1;
+            c->stats.gather_calls += 1;
+            c->stats.gather_launches += launches;
             c->stats.gathered_elems += n;
             if (c->live > c->stats.peak_live_elems) c->stats.peak_live_elems = c->live;
             return ZERO3_OK;
@@ -231,21 +248,63 @@ zero3_status gather(zero3_coordinator* c, int32_t k, bool evict) {
 }
 
 // Issues gathers for the trace entries after the current position while the
-// prefetch budget and the live budget allow.
+// prefetch budget and the live budget allow, as one batch: arena ranges for
+// every submodule first, one wait for the latest release among them, one
+// gather of all of them, then their ready events.
 zero3_status prefetch_ahead(zero3_coordinator* c) {
     if (!c->trace_ok || c->cfg.prefetch_bucket_size <= 0) return ZERO3_OK;
-    for (int64_t j = c->pos; j < static_cast<int64_t>(c->trace.size()); ++j) {
-        const int32_t k = c->trace[j];
-        if (c->off[k] >= 0) continue;  // already gathered (ahead or kept)
-        const int64_t n = numel_of(c, k);
-        if (c->ahead_elems + n > c->cfg.prefetch_bucket_size) break;
-        zero3_status st = gather(c, k, false);
-        if (st == ZERO3_ENOMEM) break;  // no room now: try again at the next fetch
-        if (st != ZERO3_OK) return st;
-        c->ahead[k] = 1;
-        c->ahead_elems += n;
-        c->stats.prefetched += 1;
+    std::vector<int32_t> ks;
+    std::vector<uint16_t*> outs;
+    uint64_t wait_seq = 0;
+    try {
+        for (int64_t j = c->pos; j < static_cast<int64_t>(c->trace.size()); ++j) {
+            const int32_t k = c->trace[j];
+            if (c->off[k] >= 0) continue;  // already gathered (ahead, kept, or in this batch)
+            const int64_t n = numel_of(c, k);
+            if (c->ahead_elems + n > c->cfg.prefetch_bucket_size) break;
+            if (c->live + n > c->cfg.max_live_parameters) break;
+            int64_t o = 0;
+            if (n > 0) {
+                uint64_t seq = 0;
+                o = free_take(c, span_of(c, k), &seq);
+                if (o < 0) break;  // no room now: try again at the next fetch
+                wait_seq = std::max(wait_seq, seq);
+            }
+            ks.push_back(k);
+            outs.push_back(c->arena + o);
+            c->off[k] = o;
+            c->live += n;
+            c->status[k] = ZERO3_INFLIGHT;
+            c->ahead[k] = 1;
+            c->ahead_elems += n;
+        }
+    } catch (const std::bad_alloc&) {
+        return ZERO3_ENOMEM;  // (ranges taken so far are accounted and stay valid)
     }
+    if (ks.empty()) return ZERO3_OK;
+    // release events of one stream complete in order: the latest covers all
+    if (wait_seq > 0 &&
+        cudaStreamWaitEvent(c->prefetch, c->rel[wait_seq % kReleaseRing], 0) != cudaSuccess)
+        return ZERO3_ECUDA;
+    int64_t launches = 0;
+    zero3_status st = z3::gather_submodules(c->plan, ks.data(), static_cast<int64_t>(ks.size()),
+                                            c->sparam.data(), c->persist, outs.data(), c->prefetch,
+                                            &launches);
+    if (st != ZERO3_OK) return st;
+    const uint64_t seq = ++c->prefetch_seq;  // every event below marks this position
+    for (int32_t k : ks) {
+        if (cudaEventRecord(c->ready[k], c->prefetch) != cudaSuccess) return ZERO3_ECUDA;
+        c->ready_seq[k] = seq;
+        const int64_t n = numel_of(c, k);
+        c->stats.prefetched += 1;
+        if (n > 0) {  // an empty submodule is a view, not a gather
+            c->stats.gathers += 1;
+            c->stats.gathered_elems += n;
+        }
+    }
+    if (c->live > c->stats.peak_live_elems) c->stats.peak_live_elems = c->live;
+    c->stats.gather_calls += 1;
+    c->stats.gather_launches += launches;
     return ZERO3_OK;
 }
 
@@ -314,6 +373,7 @@ zero3_status zero3_coordinator_create(zero3_plan* plan, const int32_t* trace, in
         c->off.assign(n_sub, -1);
         c->ahead.assign(n_sub, 0);
         c->ready.assign(n_sub, nullptr);
+        c->ready_seq.assign(n_sub, 0);
         // only whole 8-element units of the arena are handed out
         if (arena_elems >= 8) c->free_list.push_back(FreeRange{0, arena_elems / 8 * 8, 0});
     } catch (const std::bad_alloc&) {
@@ -366,7 +426,12 @@ zero3_status zero3_coordinator_fetch(zero3_coordinator* c, int32_t k, uint16_t**
         c->ahead[k] = 0;
         c->ahead_elems -= numel_of(c, k);
     }
-    if (cudaStreamWaitEvent(c->compute, c->ready[k], 0) != cudaSuccess) return ZERO3_ECUDA;
+    // skip a wait that an earlier wait on a later prefetch event implies
+    if (c->ready_seq[k] > c->compute_waited) {
+        if (cudaStreamWaitEvent(c->compute, c->ready[k], 0) != cudaSuccess) return ZERO3_ECUDA;
+        c->compute_waited = c->ready_seq[k];
+        c->stats.compute_waits += 1;
+    }
     c->refs[k] += 1;
     zero3_status st = prefetch_ahead(c);
     if (st != ZERO3_OK) return st;

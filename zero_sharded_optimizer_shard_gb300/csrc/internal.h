@@ -76,15 +76,10 @@ struct Span {
     // the widest aligned width (16, 8, 4 or 2 bytes).
     int32_t gphase;
     int32_t fphase;
-    // 1: the gradients of this span are read from StreamArgs::pgrads (the
-    // persistent group's own per-rank buffers) instead of StreamArgs::grads
-    int32_t pg;
-    int32_t pad_;
 };
 
 struct StreamArgs {
     const uint16_t* grads[ZERO3_MAX_RANKS];
-    const uint16_t* pgrads[ZERO3_MAX_RANKS];  // persistent group's gradients (spans with pg)
     uint16_t* reps[ZERO3_MAX_RANKS];   // kFusedRep: every rank's full parameter copy
     uint16_t* full;
     Span span[kMaxSpans];

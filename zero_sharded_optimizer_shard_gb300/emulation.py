@@ -5,9 +5,13 @@ device generator fills the inputs, and every step of the path is a call into
 libzero3 through the `zero3` binding.
 
 Layout (all separate allocations, each 512-byte aligned by the allocator):
-  grads[c][q]   bf16  rank q's local gradient for flat range chunk c
-                      (chunk c = [lo_c, hi_c); index f at grads[c][q][f - lo_c])
-  pgrads[q]     bf16  rank q's local gradient of the persistent group (psi_s)
+  gbufs[c][q]   bf16  rank q's local gradient buffer for flat range chunk c
+                      (chunk c = [lo_c, hi_c)); the first chunk's buffer also
+                      holds the persistent group's gradients after the flat
+                      ones (at the next 16-byte boundary), so one fused launch
+                      covers both
+  grads[c][q]   view  the flat part: index f at grads[c][q][f - lo_c]
+  pgrads[q]     view  rank q's local gradient of the persistent group (psi_s)
   master/m/v[r] fp32  rank r's optimizer-state shard (S), only for state ranks
   sparam[r]     bf16  rank r's parameter shard (S), every rank
   full          bf16  the flat all-gathered parameter buffer (psi_pad)
@@ -68,11 +72,21 @@ class Emulation:
             self.chunks = [(lo, hi)] if hi > lo else []
         bf, f32 = torch.bfloat16, torch.float32
         A = self.alloc
+        self.gbufs: List[List[torch.Tensor]] = []
         self.grads: List[List[torch.Tensor]] = []
+        self.pgrads: List[torch.Tensor] = []
         if alloc_grads:
-            for (a, b) in self.chunks:
-                self.grads.append([A(b - a, bf) for _ in range(self.nd)])
-        self.pgrads = [A(self.psi_s, bf) for _ in range(self.nd)]
+            for c, (a, b) in enumerate(self.chunks):
+                n = b - a
+                tail = (n + 7) // 8 * 8 + self.psi_s if c == 0 else n
+                bufs = [A(tail, bf) for _ in range(self.nd)]
+                self.gbufs.append(bufs)
+                self.grads.append([x[:n] for x in bufs])
+                if c == 0:
+                    o = (n + 7) // 8 * 8
+                    self.pgrads = [x[o:o + self.psi_s] for x in bufs]
+        if not self.pgrads:
+            self.pgrads = [A(self.psi_s, bf) for _ in range(self.nd)]
         self.master: List[Optional[torch.Tensor]] = [None] * self.nd
         self.m: List[Optional[torch.Tensor]] = [None] * self.nd
         self.v: List[Optional[torch.Tensor]] = [None] * self.nd

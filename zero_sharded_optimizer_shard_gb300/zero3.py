@@ -64,7 +64,8 @@ class PrefetchConfig(C.Structure):
 class CoordinatorStats(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("steps", "gathers", "prefetched", "prefetch_hits",
                                           "reuse_hits", "evictions", "trace_misses",
-                                          "gathered_elems", "peak_live_elems", "live_elems")]
+                                          "gathered_elems", "peak_live_elems", "live_elems",
+                                          "gather_calls", "gather_launches", "compute_waits")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

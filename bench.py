@@ -116,9 +116,17 @@ def peaks():
     return 6800.0, "fallback"
 
 
+FUSED_SOURCES = ("kernels.cu", "device_common.cuh", "internal.h")
+
+
 def kernels_sha() -> str:
-    p = os.path.join(ROOT, "zero_sharded_optimizer_shard_gb300", "csrc", "kernels.cu")
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    """Hash of the sources the fused kernel is compiled from (its profile
+    figures hold only while these are unchanged)."""
+    h = hashlib.sha256()
+    for name in FUSED_SOURCES:
+        p = os.path.join(ROOT, "zero_sharded_optimizer_shard_gb300", "csrc", name)
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def profile_traffic(workload: str, sha: str):
@@ -129,7 +137,7 @@ def profile_traffic(workload: str, sha: str):
         return None
     with open(PROFILE_JSON) as f:
         d = json.load(f)
-    if d.get("kernels_cu_sha16") != sha:
+    if d.get("fused_sources_sha16") != sha:
         return None
     v = d.get("traffic_bytes_per_launch", {}).get(workload)
     return float(v) if v is not None else None
@@ -914,8 +922,8 @@ def measure(args, name, world, local, with_e2e, with_cpu):
                      "nominal_peak": NOMINAL_HBM_GBS,
                      "nominal_note": "GB300 HBM3e nominal bandwidth (NVIDIA product figure)",
                      "traffic": traffic,
-                     "traffic_source": (os.path.relpath(PROFILE_JSON, ROOT) + f" (kernels.cu "
-                                        f"{sha})") if traffic is not None else None,
+                     "traffic_source": (os.path.relpath(PROFILE_JSON, ROOT) + f" (fused kernel "
+                                        f"sources {sha})") if traffic is not None else None,
                      "kernel": "stream_kernel<kFused, N_d> (zero3_step)"},
         "gpu_launches": (n_fused + n_gather) * args.steps,
         "clocks": clk,

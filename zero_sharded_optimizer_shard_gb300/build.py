@@ -28,10 +28,12 @@ COMMON = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC"
           f"-I{INCLUDE}"]
 
 LIBS = {
-    "libzero3.so": ["plan.cpp", "api.cpp", "checkpoint.cpp", "coordinator.cpp", "kernels.cu"],
+    "libzero3.so": ["plan.cpp", "api.cpp", "checkpoint.cpp", "coordinator.cpp", "kernels.cu",
+                    "pieces.cu"],
     "libzero3_synth.so": ["synth.cu"],
 }
-HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(INCLUDE, "zero3.h")]
+HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(CSRC, "device_common.cuh"),
+           os.path.join(INCLUDE, "zero3.h")]
 
 
 def nvcc() -> str:

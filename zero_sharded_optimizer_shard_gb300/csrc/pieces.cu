@@ -1,0 +1,305 @@
+// The piece kernel of the copy-like launches (sm_103a): submodule gathers
+// (one or several submodules per launch), the all-gather copy of the shards
+// into the flat parameter buffer, and the dequantizing qwZ all-gather.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace z3 {
+
+// Kernel parameters are passed by value; 32764 bytes is the limit.
+static_assert(sizeof(PieceArgs<kLargePieces>) <= 32764, "PieceArgs exceeds the kernel parameter limit");
+
+namespace {
+
+// Copy-like work: submodule gathers (one or many submodules per launch), the
+// all-gather copy sparam -> full and the dequantizing qwZ all-gather.  Every
+// byte moves once, so the kernel is bound by HBM bandwidth with few
+// operations per byte; what matters is many independent 16-byte requests in
+// flight and no narrow or partial accesses.
+//
+// Chunks are aligned to the DESTINATION, so every store is one aligned
+// 16-byte store; a source at a nonzero phase is realigned on the way in.
+// A warp's 32 lanes hold 32 consecutive chunks of one piece (per step j of
+// the thread's four chunks), so lane l loads the aligned source unit under
+// its chunk and takes lane l+1's by shuffle (lane 31 loads the one after):
+// one aligned load per chunk.  Chunks whose source units would reach past
+// either end of the piece (at most two per piece edge) are copied element by
+// element.  Each lane issues all of its loads before its first store (the
+// compiler cannot move a load above a store through a possibly aliasing
+// pointer, which would leave one load in flight per lane).
+constexpr int kPieceChunks = kPieceWarpChunks / 32;   // chunks per lane
+
+// Source unit of a chunk and its realignment, per kind.
+//   bf16: 8 elements per aligned 16-byte unit; PH elements.
+//   int8: 8 codes per aligned 8-byte unit; PH bytes.
+//   int4: 8 codes per aligned 4-byte unit; PH nibbles.
+// The phase is the same for a whole piece, hence for a whole warp, so the
+// realignment is compiled per phase: a few funnel shifts of fixed words.
+template <int KIND>
+struct Unit;
+template <>
+struct Unit<kPieceBf16> {
+    using T = uint4;
+    static __device__ __forceinline__ T load(const void* src, int64_t idx) {
+        return ldcs16(static_cast<const uint16_t*>(src) + idx);
+    }
+    static __device__ __forceinline__ T shfl(const T& x) {
+        T n;
+        n.x = __shfl_down_sync(0xffffffffu, x.x, 1);
+        n.y = __shfl_down_sync(0xffffffffu, x.y, 1);
+        n.z = __shfl_down_sync(0xffffffffu, x.z, 1);
+        n.w = __shfl_down_sync(0xffffffffu, x.w, 1);
+        return n;
+    }
+    // elements PH..PH+7 of the 16 elements a, b: words k..k+4 (k = PH / 2)
+    // funnel-shifted right by 16 * (PH % 2) bits
+    template <int PH>
+    static __device__ __forceinline__ T realign(const T& a, const T& b) {
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        constexpr int k = PH / 2;
+        constexpr uint32_t sh = (PH & 1) * 16u;
+        if constexpr (sh == 0) return make_uint4(w[k], w[k + 1], w[k + 2], w[k + 3]);
+        return make_uint4(__funnelshift_r(w[k], w[k + 1], sh), __funnelshift_r(w[k + 1], w[k + 2], sh),
+                          __funnelshift_r(w[k + 2], w[k + 3], sh),
+                          __funnelshift_r(w[k + 3], w[k + 4], sh));
+    }
+};
+template <>
+struct Unit<kPieceInt8> {
+    using T = uint2;
+    static __device__ __forceinline__ T load(const void* src, int64_t idx) {
+        return __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(src) + idx));
+    }
+    static __device__ __forceinline__ T shfl(const T& x) {
+        return make_uint2(__shfl_down_sync(0xffffffffu, x.x, 1),
+                          __shfl_down_sync(0xffffffffu, x.y, 1));
+    }
+    // bytes PH..PH+7 of the 16 bytes a, b
+    template <int PH>
+    static __device__ __forceinline__ T realign(const T& a, const T& b) {
+        const uint32_t w[4] = {a.x, a.y, b.x, b.y};
+        constexpr int k = PH / 4;
+        constexpr uint32_t sh = (PH & 3) * 8u;
+        if constexpr (sh == 0) return make_uint2(w[k], w[k + 1]);
+        return make_uint2(__funnelshift_r(w[k], w[k + 1], sh), __funnelshift_r(w[k + 1], w[k + 2], sh));
+    }
+};
+template <>
+struct Unit<kPieceInt4> {
+    using T = uint32_t;
+    static __device__ __forceinline__ T load(const void* src, int64_t idx) {
+        return __ldcs(static_cast<const unsigned int*>(src) + idx / 8);
+    }
+    static __device__ __forceinline__ T shfl(const T& x) {
+        return __shfl_down_sync(0xffffffffu, x, 1);
+    }
+    template <int PH>
+    static __device__ __forceinline__ T realign(const T& a, const T& b) {
+        return __funnelshift_r(a, b, PH * 4u);
+    }
+};
+
+// Exact binary32 value of a code without a conversion instruction: the code
+// plus a bias (128 for int8, 8 for int4) is an integer below 2^8, placed in
+// the low mantissa bits of 2^23; subtracting 2^23 + bias is exact.
+__device__ __forceinline__ float int8_code_f32(uint32_t biased_word, int k) {
+    // byte k of the biased word under the exponent byte 0x4B (2^23)
+    const uint32_t v = __byte_perm(biased_word, 0x4B000000u, 0x7650u | static_cast<uint32_t>(k));
+    return __fsub_rn(__uint_as_float(v), 8388736.0f);  // 2^23 + 128
+}
+__device__ __forceinline__ float int4_code_f32(uint32_t biased_word, int k) {
+    const uint32_t v = ((biased_word >> (4 * k)) & 0xfu) | 0x4B000000u;
+    return __fsub_rn(__uint_as_float(v), 8388616.0f);  // 2^23 + 8
+}
+
+// Code e (0..7) of a realigned unit as binary32.
+template <int KIND>
+__device__ __forceinline__ float code_f32(const typename Unit<KIND>::T& u, int e) {
+    if constexpr (KIND == kPieceInt4)
+        return int4_code_f32(u ^ 0x88888888u, e);
+    else
+        return int8_code_f32((e < 4 ? u.x : u.y) ^ 0x80808080u, e & 3);
+}
+
+// Destination element d of piece P, element by element (chunks at the
+// piece's edges).
+template <int KIND>
+__device__ __forceinline__ uint16_t piece_element(const Piece& P, int64_t d) {
+    const int64_t e = P.s0 + d;
+    if constexpr (KIND == kPieceBf16) {
+        return static_cast<const uint16_t*>(P.src)[e];
+    } else {
+        int c;
+        if constexpr (KIND == kPieceInt4) {
+            const uint32_t b = static_cast<const uint8_t*>(P.src)[e / 2];
+            c = static_cast<int>(b << (28 - 4 * (e & 1))) >> 28;
+        } else {
+            c = static_cast<const int8_t*>(P.src)[e];
+        }
+        return to_bf16(__fmul_rn(static_cast<float>(c), P.scales[e / kQwzBlock]));
+    }
+}
+
+// Phase 2 of a warp's chunks at source phase PH: take the neighbour's unit
+// by shuffle (lane 31 loaded its own), realign, convert and store the vector
+// chunks.  Every lane of the warp calls this (the shuffles need all of
+// them).
+// Dequantizing kinds: y = bf16_rne(f32(code) * scale), with each element's
+// own 256-element block scale; only a chunk whose source starts in the last
+// 7 elements of a block (possible when PH != 0) straddles two blocks, and it
+// redoes its tail with the second scale.
+template <int KIND, int PH>
+__device__ __forceinline__ void piece_phase2(const Piece& P, int lane, int64_t c0,
+                                             typename Unit<KIND>::T* cur,
+                                             const typename Unit<KIND>::T* nxt, const bool* vec,
+                                             const float* sc0, const float* sc1) {
+    using U = Unit<KIND>;
+#pragma unroll
+    for (int j = 0; j < kPieceChunks; ++j) {
+        typename U::T u = cur[j];
+        if constexpr (PH != 0) {
+            const typename U::T n = U::shfl(cur[j]);
+            u = U::template realign<PH>(cur[j], lane == 31 ? nxt[j] : n);
+        }
+        if (!vec[j]) continue;
+        const int64_t d0 = (c0 + 32 * j) * 8;
+        uint4 x;
+        if constexpr (KIND == kPieceBf16) {
+            x = u;
+        } else {
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(code_f32<KIND>(u, e), sc0[j]);
+            if constexpr (PH != 0) {
+                // position of the chunk's first code in its block (low bits
+                // of the nonnegative source index)
+                const uint32_t in_block =
+                    (static_cast<uint32_t>(P.s0) + static_cast<uint32_t>(d0)) % kQwzBlock;
+                if (in_block > kQwzBlock - 8) {  // rare: the chunk straddles two blocks
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (e >= static_cast<int>(kQwzBlock - in_block))
+                            y[e] = __fmul_rn(code_f32<KIND>(u, e), sc1[j]);
+                }
+            }
+            x = pack8(y);
+        }
+        // plain stores: evict-first stores measured slower for the
+        // dequantizing all-gather (0.71 against 0.66 ms at 1.3B)
+        *reinterpret_cast<uint4*>(P.dst + d0) = x;
+    }
+}
+
+// PHASED: some piece of the launch has a nonzero source phase; the aligned
+// instantiation has no shuffles and fewer registers.
+template <int KIND, bool PHASED, int MAXP>
+__global__ void __launch_bounds__(kThreads, PHASED ? 4 : 5)
+    piece_kernel(const __grid_constant__ PieceArgs<MAXP> a) {
+    wait_prior_grids();
+    allow_next_grid();
+    using U = Unit<KIND>;
+    const uint32_t w = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    if (w >= a.warp0[a.n]) return;  // whole warps leave together
+    // the piece of warp w: the last i with warp0[i] <= w (same for every lane)
+    int lo = 0, hi = a.n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.warp0[mid] <= w)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const Piece& P = a.piece[lo];
+    const int lane = threadIdx.x & 31;
+    const int ph = PHASED ? P.ph : 0;
+    const int64_t c0 = static_cast<int64_t>(w - a.warp0[lo]) * kPieceWarpChunks + lane;
+    typename U::T cur[kPieceChunks], nxt[kPieceChunks];
+    bool vec[kPieceChunks];
+    float sc0[kPieceChunks], sc1[kPieceChunks];
+    // Phase 1: every load of the vector chunks (codes or values, block
+    // scales).
+#pragma unroll
+    for (int j = 0; j < kPieceChunks; ++j) {
+        const int64_t d0 = (c0 + 32 * j) * 8;
+        // the source unit under the chunk starts at destination index b
+        const int64_t b = d0 - ph;
+        vec[j] = b >= P.lo && b + (ph ? 16 : 8) <= P.hi;
+        if (b >= P.lo && b + 8 <= P.hi) cur[j] = U::load(P.src, P.s0 + b);
+        if (PHASED && ph && lane == 31 && vec[j]) nxt[j] = U::load(P.src, P.s0 + b + 8);
+        if constexpr (KIND != kPieceBf16) {
+            if (vec[j]) {
+                const uint64_t blk = static_cast<uint64_t>(P.s0 + d0) / kQwzBlock;  // >= 0
+                sc0[j] = P.scales[blk];
+                // the last element's block: the same one unless a phased
+                // chunk straddles two blocks
+                if constexpr (PHASED)
+                    sc1[j] = P.scales[static_cast<uint64_t>(P.s0 + d0 + 7) / kQwzBlock];
+            }
+        }
+    }
+    if constexpr (!PHASED) {
+        piece_phase2<KIND, 0>(P, lane, c0, cur, nxt, vec, sc0, sc1);
+    } else {
+        switch (ph) {  // warp-uniform
+            case 0: piece_phase2<KIND, 0>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
+            case 1: piece_phase2<KIND, 1>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
+            case 2: piece_phase2<KIND, 2>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
+            case 3: piece_phase2<KIND, 3>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
+            case 4: piece_phase2<KIND, 4>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
+            case 5: piece_phase2<KIND, 5>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
+            case 6: piece_phase2<KIND, 6>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
+            default: piece_phase2<KIND, 7>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
+        }
+    }
+    // Phase 3: the chunks at the piece's edges, element by element.  Kept out
+    // of the load phase: with its stores between the loads, the loads of the
+    // later chunks were no longer all in flight together (measured: the int8
+    // dequantizing all-gather at 1.3B took 0.84 ms instead of 0.66 ms).
+#pragma unroll
+    for (int j = 0; j < kPieceChunks; ++j) {
+        if (vec[j]) continue;
+        const int64_t d0 = (c0 + 32 * j) * 8;
+        const int64_t e0 = d0 > P.lo ? d0 : P.lo;
+        const int64_t e1 = d0 + 8 < P.hi ? d0 + 8 : P.hi;
+        for (int64_t d = e0; d < e1; ++d) P.dst[d] = piece_element<KIND>(P, d);
+    }
+}
+
+template <int KIND, int MAXP>
+cudaError_t launch_pieces(const PieceArgs<MAXP>& a, cudaStream_t stream) {
+    const uint32_t warps = a.warp0[a.n];
+    if (a.n <= 0 || warps == 0) return cudaSuccess;
+    const int grid = static_cast<int>((warps + kThreads / 32 - 1) / (kThreads / 32));
+    bool phased = false;
+    for (int i = 0; i < a.n; ++i) phased = phased || a.piece[i].ph != 0;
+    const cudaError_t e =
+        phased ? launch_programmatic(piece_kernel<KIND, true, MAXP>, grid, a, stream)
+               : launch_programmatic(piece_kernel<KIND, false, MAXP>, grid, a, stream);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int MAXP>
+cudaError_t launch_pieces_kind(int kind, const PieceArgs<MAXP>& a, cudaStream_t stream) {
+    switch (kind) {
+        case kPieceBf16: return launch_pieces<kPieceBf16>(a, stream);
+        case kPieceInt8: return launch_pieces<kPieceInt8>(a, stream);
+        case kPieceInt4: return launch_pieces<kPieceInt4>(a, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_pieces_small(int kind, const PieceArgs<kSmallPieces>& a, cudaStream_t stream) {
+    return launch_pieces_kind(kind, a, stream);
+}
+
+cudaError_t launch_pieces_large(int kind, const PieceArgs<kLargePieces>& a, cudaStream_t stream) {
+    return launch_pieces_kind(kind, a, stream);
+}
+
+}  // namespace z3

@@ -150,8 +150,9 @@ __device__ __forceinline__ uint16_t piece_element(const Piece& P, int64_t d) {
 // them).
 // Dequantizing kinds: y = bf16_rne(f32(code) * scale), with each element's
 // own 256-element block scale; only a chunk whose source starts in the last
-// 7 elements of a block (possible when PH != 0) straddles two blocks, and it
-// redoes its tail with the second scale.
+// 7 elements of a block (possible when PH != 0) straddles two blocks, and its
+// tail takes the second scale (a select per element: measured cheaper than a
+// fix-up branch, which the compiler predicates).
 template <int KIND, int PH>
 __device__ __forceinline__ void piece_phase2(const Piece& P, int lane, int64_t c0,
                                              typename Unit<KIND>::T* cur,
@@ -171,21 +172,18 @@ __device__ __forceinline__ void piece_phase2(const Piece& P, int lane, int64_t c
         if constexpr (KIND == kPieceBf16) {
             x = u;
         } else {
-            float y[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(code_f32<KIND>(u, e), sc0[j]);
+            // elements of the chunk in its first block: all 8 unless a
+            // phased chunk's source starts in the block's last 7 elements
+            int split = 8;
             if constexpr (PH != 0) {
-                // position of the chunk's first code in its block (low bits
-                // of the nonnegative source index)
                 const uint32_t in_block =
                     (static_cast<uint32_t>(P.s0) + static_cast<uint32_t>(d0)) % kQwzBlock;
-                if (in_block > kQwzBlock - 8) {  // rare: the chunk straddles two blocks
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        if (e >= static_cast<int>(kQwzBlock - in_block))
-                            y[e] = __fmul_rn(code_f32<KIND>(u, e), sc1[j]);
-                }
+                if (in_block > kQwzBlock - 8) split = static_cast<int>(kQwzBlock - in_block);
             }
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                y[e] = __fmul_rn(code_f32<KIND>(u, e), e < split ? sc0[j] : sc1[j]);
             x = pack8(y);
         }
         // plain stores: evict-first stores measured slower for the

@@ -1,6 +1,7 @@
 """GPU parity at the workloads' full sizes, in the launch configuration the
-benchmark uses, on sampled outputs the oracle computes one by one
-(elementwise independence of the update), plus the whole persistent group.
+benchmark uses (bucketed gathers, the persistent group in the first fused
+launch), on sampled outputs the oracle computes one by one (elementwise
+independence of the update), plus the whole persistent group.
 
 Sample: random flat indices plus every rank's first and last two local
 indices, tensor boundaries and the padding."""
@@ -88,15 +89,72 @@ def check_persistent(e, ps):
 
 
 def run(w, T, grad_step=None, **kw):
+    """T steps as the benchmark runs them: the forward and backward gathers
+    in all-gather buckets of the workload's size, then the fused step with the
+    persistent group in its first launch."""
     from zero_sharded_optimizer_shard_gb300.emulation import Emulation
     e = Emulation(w, **kw)
     e.init_params()
     for t in range(1, T + 1):
         if grad_step is None or t == 1:
             e.fill_grads(t if grad_step is None else grad_step)
-        e.full_step(t)
+        e.forward_backward_gathers(bucket=w.gather_bucket)
+        e.step(t)
     torch.cuda.synchronize()
     return e
+
+
+def check_fetch_many(e, plan, w, T, grad_step, groups, persist_values, state_ranks=None,
+                     n=2000, seed=7):
+    """zero3_fetch_submodules over the benchmark's all-gather buckets: each
+    submodule's gathered buffer at sampled positions (and its ends) against
+    the oracle's bf16 parameters of the same elements.  Ranks outside
+    state_ranks hold their initial shards (cast from the initial masters);
+    persist_values(pidx) gives the persistent group's bf16 values."""
+    from zero_sharded_optimizer_shard_gb300 import synth
+    from zero_sharded_optimizer_shard_gb300.workloads import STREAM_MASTER
+    rng = np.random.default_rng(seed)
+    S = plan.shard_len
+    for ks in groups:
+        outs = e.fetch_many(ks)
+        torch.cuda.synchronize()
+        base_ptr = e.arena.data_ptr()
+        for k, o in zip(ks, outs):
+            members = plan.submodules.get(k, [])
+            pos, flat, pers = [], [], []
+            base = 0
+            for t in members:
+                nt = plan.numel[t]
+                if nt == 0:
+                    continue
+                js = np.unique(np.concatenate([rng.integers(0, nt, min(nt, n // len(members) + 1)),
+                                               [0, nt - 1]]))
+                for j in js:
+                    pos.append(base + j)
+                    flat.append(-1 if plan.persistent[t] else plan.offset[t] + j)
+                    pers.append(plan.offset[t] + j if plan.persistent[t] else -1)
+                base += nt
+            if not pos:
+                continue
+            pos, flat, pers = np.array(pos), np.array(flat), np.array(pers)
+            off = (o - base_ptr) // 2
+            got = u16(e.arena[torch.from_numpy(off + pos).to(e.arena.device)])
+            want = np.empty(len(pos), np.uint16)
+            fsel = flat >= 0
+            upd = fsel.copy()
+            if state_ranks is not None:
+                upd &= np.isin(flat // S, state_ranks)
+            if upd.any():
+                want[upd] = sampled_oracle(w, plan, flat[upd], T, grad_step)[3]
+            init = fsel & ~upd
+            if init.any():
+                want[init] = O.bf16_rne(synth.normal_f32(w.seed, STREAM_MASTER, 0, 0, flat[init],
+                                                         w.master_sigma))
+            if (~fsel).any():
+                want[~fsel] = persist_values(pers[~fsel])
+            assert np.array_equal(got, want), f"submodule {k}"
+        for k in ks:
+            e.release(k)
 
 
 def check_fetch(e, plan, w, T, grad_step, ks, ps, n=4000, seed=0):
@@ -156,6 +214,9 @@ def test_decoder_1p3b_bench_configuration():
     ps = persistent_oracle(w, plan, T, grad_step=1)
     check_persistent(e, ps)
     check_fetch(e, plan, w, T, 1, [0, 12, plan.n_submodules - 1], ps)
+    groups = e.gather_buckets(w.gather_bucket)
+    assert len(groups) >= 2
+    check_fetch_many(e, plan, w, T, 1, [groups[0], groups[-1]], lambda i: ps.param[i])
 
 
 def test_llama_7b_rank0_view():
@@ -169,6 +230,11 @@ def test_llama_7b_rank0_view():
     check_sample(e, plan, w, sample_indices(plan, 0, plan.shard_len, 100_000, 3), T)
     ps = persistent_oracle(w, plan, T)
     check_persistent(e, ps)
+    # the bench's bucketed gathers: the first bucket (embeddings and the first
+    # layer, mostly rank 0) and the last (final layers and the head, other ranks)
+    groups = e.gather_buckets(w.gather_bucket)
+    check_fetch_many(e, plan, w, T, None, [groups[0], groups[-1]], lambda i: ps.param[i],
+                     state_ranks=[0], n=600)
 
 
 def test_ragged_2000_full():
@@ -198,6 +264,10 @@ def test_ragged_2000_full():
         need = np.unique(np.concatenate(need))
         ps_param[need] = sampled_persistent_oracle(w, plan, need, T)[3]
     check_fetch(e, plan, w, T, None, ks, O.PersistState(None, None, None, ps_param))
+    # the bench's bucketed gathers (several 512-piece launches per call)
+    groups = e.gather_buckets(w.gather_bucket)
+    check_fetch_many(e, plan, w, T, None, [groups[0]],
+                     lambda i: sampled_persistent_oracle(w, plan, i, T)[3], n=200)
 
 
 def test_llama_7b_full_emulation_max_size():

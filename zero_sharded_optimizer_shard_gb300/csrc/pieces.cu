@@ -44,9 +44,11 @@ struct Unit;
 template <>
 struct Unit<kPieceBf16> {
     using T = uint4;
-    static __device__ __forceinline__ T load(const void* src, int64_t idx) {
-        return ldcs16(static_cast<const uint16_t*>(src) + idx);
+    static constexpr int kUnitBytes = 16;  // bytes of 8 source elements
+    static __device__ __forceinline__ const char* at(const void* src, int64_t idx) {
+        return static_cast<const char*>(src) + idx * 2;
     }
+    static __device__ __forceinline__ T load(const char* p) { return ldcs16(p); }
     static __device__ __forceinline__ T shfl(const T& x) {
         T n;
         n.x = __shfl_down_sync(0xffffffffu, x.x, 1);
@@ -71,8 +73,12 @@ struct Unit<kPieceBf16> {
 template <>
 struct Unit<kPieceInt8> {
     using T = uint2;
-    static __device__ __forceinline__ T load(const void* src, int64_t idx) {
-        return __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(src) + idx));
+    static constexpr int kUnitBytes = 8;
+    static __device__ __forceinline__ const char* at(const void* src, int64_t idx) {
+        return static_cast<const char*>(src) + idx;
+    }
+    static __device__ __forceinline__ T load(const char* p) {
+        return __ldcs(reinterpret_cast<const uint2*>(p));
     }
     static __device__ __forceinline__ T shfl(const T& x) {
         return make_uint2(__shfl_down_sync(0xffffffffu, x.x, 1),
@@ -91,8 +97,13 @@ struct Unit<kPieceInt8> {
 template <>
 struct Unit<kPieceInt4> {
     using T = uint32_t;
-    static __device__ __forceinline__ T load(const void* src, int64_t idx) {
-        return __ldcs(static_cast<const unsigned int*>(src) + idx / 8);
+    static constexpr int kUnitBytes = 4;
+    // idx is a multiple of 8 wherever a unit is read (an aligned unit)
+    static __device__ __forceinline__ const char* at(const void* src, int64_t idx) {
+        return static_cast<const char*>(src) + idx / 2;
+    }
+    static __device__ __forceinline__ T load(const char* p) {
+        return __ldcs(reinterpret_cast<const unsigned int*>(p));
     }
     static __device__ __forceinline__ T shfl(const T& x) {
         return __shfl_down_sync(0xffffffffu, x, 1);
@@ -154,11 +165,19 @@ __device__ __forceinline__ uint16_t piece_element(const Piece& P, int64_t d) {
 // tail takes the second scale (a select per element: measured cheaper than a
 // fix-up branch, which the compiler predicates).
 template <int KIND, int PH>
-__device__ __forceinline__ void piece_phase2(const Piece& P, int lane, int64_t c0,
+__device__ __forceinline__ void piece_phase2(uint16_t* dst, int64_t x0, int lane,
                                              typename Unit<KIND>::T* cur,
                                              const typename Unit<KIND>::T* nxt, const bool* vec,
                                              const float* sc0, const float* sc1) {
     using U = Unit<KIND>;
+    // elements of a chunk in its first block: all 8 unless a phased chunk's
+    // source starts in the block's last 7 elements (the same for the lane's
+    // four chunks, which lie 256 elements apart)
+    int split = 8;
+    if constexpr (PH != 0 && KIND != kPieceBf16) {
+        const uint32_t in_block = static_cast<uint32_t>(x0) % kQwzBlock;  // x0 >= 0
+        if (in_block > kQwzBlock - 8) split = static_cast<int>(kQwzBlock - in_block);
+    }
 #pragma unroll
     for (int j = 0; j < kPieceChunks; ++j) {
         typename U::T u = cur[j];
@@ -167,19 +186,10 @@ __device__ __forceinline__ void piece_phase2(const Piece& P, int lane, int64_t c
             u = U::template realign<PH>(cur[j], lane == 31 ? nxt[j] : n);
         }
         if (!vec[j]) continue;
-        const int64_t d0 = (c0 + 32 * j) * 8;
         uint4 x;
         if constexpr (KIND == kPieceBf16) {
             x = u;
         } else {
-            // elements of the chunk in its first block: all 8 unless a
-            // phased chunk's source starts in the block's last 7 elements
-            int split = 8;
-            if constexpr (PH != 0) {
-                const uint32_t in_block =
-                    (static_cast<uint32_t>(P.s0) + static_cast<uint32_t>(d0)) % kQwzBlock;
-                if (in_block > kQwzBlock - 8) split = static_cast<int>(kQwzBlock - in_block);
-            }
             float y[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -188,7 +198,7 @@ __device__ __forceinline__ void piece_phase2(const Piece& P, int lane, int64_t c
         }
         // plain stores: evict-first stores measured slower for the
         // dequantizing all-gather (0.71 against 0.66 ms at 1.3B)
-        *reinterpret_cast<uint4*>(P.dst + d0) = x;
+        *reinterpret_cast<uint4*>(dst + 256 * j) = x;
     }
 }
 
@@ -214,56 +224,92 @@ __global__ void __launch_bounds__(kThreads, PHASED ? 4 : 5)
     const Piece& P = a.piece[lo];
     const int lane = threadIdx.x & 31;
     const int ph = PHASED ? P.ph : 0;
-    const int64_t c0 = static_cast<int64_t>(w - a.warp0[lo]) * kPieceWarpChunks + lane;
+    // destination index of the warp's first element, and of the lane's chunk
+    // at step 0 (step j adds 256: 32 lanes of 8 elements)
+    const int64_t wbase = static_cast<int64_t>(w - a.warp0[lo]) * (kPieceWarpChunks * 8);
+    const int64_t d00 = wbase + 8 * lane;
+    const int64_t x0 = P.s0 + d00;  // its source index
+    const char* src = U::at(P.src, x0 - ph);  // the aligned source unit under it
+    constexpr int kStep = 32 * U::kUnitBytes;
     typename U::T cur[kPieceChunks], nxt[kPieceChunks];
     bool vec[kPieceChunks];
     float sc0[kPieceChunks], sc1[kPieceChunks];
     // Phase 1: every load of the vector chunks (codes or values, block
-    // scales).
+    // scales).  A warp whose 1024 elements and the units around them lie
+    // inside the piece (nearly all warps) needs no per-chunk bounds.
+    const bool interior = wbase >= P.lo + 8 && wbase + kPieceWarpChunks * 8 + 8 <= P.hi;
+    if (interior) {
 #pragma unroll
-    for (int j = 0; j < kPieceChunks; ++j) {
-        const int64_t d0 = (c0 + 32 * j) * 8;
-        // the source unit under the chunk starts at destination index b
-        const int64_t b = d0 - ph;
-        vec[j] = b >= P.lo && b + (ph ? 16 : 8) <= P.hi;
-        if (b >= P.lo && b + 8 <= P.hi) cur[j] = U::load(P.src, P.s0 + b);
-        if (PHASED && ph && lane == 31 && vec[j]) nxt[j] = U::load(P.src, P.s0 + b + 8);
-        if constexpr (KIND != kPieceBf16) {
-            if (vec[j]) {
-                const uint64_t blk = static_cast<uint64_t>(P.s0 + d0) / kQwzBlock;  // >= 0
-                sc0[j] = P.scales[blk];
-                // the last element's block: the same one unless a phased
-                // chunk straddles two blocks
-                if constexpr (PHASED)
-                    sc1[j] = P.scales[static_cast<uint64_t>(P.s0 + d0 + 7) / kQwzBlock];
+        for (int j = 0; j < kPieceChunks; ++j) {
+            vec[j] = true;
+            cur[j] = U::load(src + j * kStep);
+            if (PHASED && ph && lane == 31) nxt[j] = U::load(src + j * kStep + U::kUnitBytes);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < kPieceChunks; ++j) {
+            // the source unit under the chunk starts at destination index b
+            const int64_t b = d00 + 256 * j - ph;
+            vec[j] = b >= P.lo && b + (ph ? 16 : 8) <= P.hi;
+            if (b >= P.lo && b + 8 <= P.hi) cur[j] = U::load(src + j * kStep);
+            if (PHASED && ph && lane == 31 && vec[j])
+                nxt[j] = U::load(src + j * kStep + U::kUnitBytes);
+        }
+    }
+    // Block scales of the vector chunks: the chunk's first element's block,
+    // and its last element's (the same one unless a phased chunk straddles
+    // two blocks).
+    if constexpr (KIND != kPieceBf16) {
+        if (interior) {
+            // x0 >= 0: the warp starts past the piece's first element
+            const float* s0p = P.scales + static_cast<uint64_t>(x0) / kQwzBlock;
+            const float* s1p = P.scales + static_cast<uint64_t>(x0 + 7) / kQwzBlock;
+#pragma unroll
+            for (int j = 0; j < kPieceChunks; ++j) {
+                sc0[j] = s0p[j];
+                if constexpr (PHASED) sc1[j] = s1p[j];
+            }
+        } else {
+            // x0 itself may lie before the piece (negative) on an edge lane;
+            // a vector chunk's own source index x0 + 256 j never does
+#pragma unroll
+            for (int j = 0; j < kPieceChunks; ++j) {
+                if (vec[j]) {
+                    const uint64_t xj = static_cast<uint64_t>(x0 + 256 * j);
+                    sc0[j] = P.scales[xj / kQwzBlock];
+                    if constexpr (PHASED) sc1[j] = P.scales[(xj + 7) / kQwzBlock];
+                }
             }
         }
     }
+    uint16_t* dst = P.dst + d00;
     if constexpr (!PHASED) {
-        piece_phase2<KIND, 0>(P, lane, c0, cur, nxt, vec, sc0, sc1);
+        piece_phase2<KIND, 0>(dst, x0, lane, cur, nxt, vec, sc0, sc1);
     } else {
         switch (ph) {  // warp-uniform
-            case 0: piece_phase2<KIND, 0>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
-            case 1: piece_phase2<KIND, 1>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
-            case 2: piece_phase2<KIND, 2>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
-            case 3: piece_phase2<KIND, 3>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
-            case 4: piece_phase2<KIND, 4>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
-            case 5: piece_phase2<KIND, 5>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
-            case 6: piece_phase2<KIND, 6>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
-            default: piece_phase2<KIND, 7>(P, lane, c0, cur, nxt, vec, sc0, sc1); break;
+            case 0: piece_phase2<KIND, 0>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
+            case 1: piece_phase2<KIND, 1>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
+            case 2: piece_phase2<KIND, 2>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
+            case 3: piece_phase2<KIND, 3>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
+            case 4: piece_phase2<KIND, 4>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
+            case 5: piece_phase2<KIND, 5>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
+            case 6: piece_phase2<KIND, 6>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
+            default: piece_phase2<KIND, 7>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
         }
     }
     // Phase 3: the chunks at the piece's edges, element by element.  Kept out
     // of the load phase: with its stores between the loads, the loads of the
     // later chunks were no longer all in flight together (measured: the int8
     // dequantizing all-gather at 1.3B took 0.84 ms instead of 0.66 ms).
+    if (!interior) {
 #pragma unroll
-    for (int j = 0; j < kPieceChunks; ++j) {
-        if (vec[j]) continue;
-        const int64_t d0 = (c0 + 32 * j) * 8;
-        const int64_t e0 = d0 > P.lo ? d0 : P.lo;
-        const int64_t e1 = d0 + 8 < P.hi ? d0 + 8 : P.hi;
-        for (int64_t d = e0; d < e1; ++d) P.dst[d] = piece_element<KIND>(P, d);
+        for (int j = 0; j < kPieceChunks; ++j) {
+            if (vec[j]) continue;
+            const int64_t d0 = d00 + 256 * j;
+            const int64_t e0 = d0 > P.lo ? d0 : P.lo;
+            const int64_t e1 = d0 + 8 < P.hi ? d0 + 8 : P.hi;
+            for (int64_t d = e0; d < e1; ++d) P.dst[d] = piece_element<KIND>(P, d);
+        }
     }
 }
 

@@ -123,3 +123,20 @@ def test_second_workload_in_the_same_line():
     assert c["config"]["name"] == "ragged" and c["value"] > 0
     assert 0 < c["roofline"]["frac"] < 2 and c["cpu_baseline"]["value"] > 0
     assert c["e2e"]["value"] > 0 and set(c["rows"]) == {"a1_a4_fused", "a5_gathers"}
+
+
+def test_fused_profile_matches_the_current_sources():
+    """The committed ncu traffic figure belongs to the fused kernel as it is
+    now: its JSON is keyed by the hash of the kernel's sources, and the
+    bench reads it (for both workloads of the default run) only on a match."""
+    sys.path.insert(0, ROOT)
+    import bench
+    d = json.load(open(bench.PROFILE_JSON))
+    assert d["fused_sources_sha16"] == bench.kernels_sha()
+    for name in ("decoder_1p3b", "llama_7b_rank0"):
+        t = bench.profile_traffic(name, bench.kernels_sha())
+        assert t is not None and t > 0
+    # within a few per cent of the algorithmic bytes of one launch
+    alg_1p3b = 1_315_080_192 * 44 + 643_072 * 42
+    assert 0.95 < bench.profile_traffic("decoder_1p3b", bench.kernels_sha()) / alg_1p3b < 1.02
+    assert bench.profile_traffic("decoder_1p3b", "0" * 16) is None

@@ -400,6 +400,17 @@ def test_zero_size_tensors(dev):
         n = plan.submodule_numel(k)
         assert np.array_equal(u16(e.out)[:n], O.fetch_submodule(plan, k, st.sparam, ps.param))
         e.release(k)
+    # every submodule in one call, the empty one (only zero-size tensors) included
+    ks = list(range(plan.n_submodules))
+    outs = e.fetch_many(ks)
+    torch.cuda.synchronize()
+    for k, o in zip(ks, outs):
+        n = plan.submodule_numel(k)
+        off = (o - e.arena.data_ptr()) // 2
+        assert np.array_equal(u16(e.arena)[off:off + n],
+                              O.fetch_submodule(plan, k, st.sparam, ps.param)), k
+        assert zero3.zero3_submodule_status(e.plan, k) != zero3.NOT_AVAILABLE
+        e.release(k)
 
 
 # ---------------------------------------------------------------- every phase

@@ -366,6 +366,18 @@ def oracle_on_cores(s, inputs, n_steps: int, procs: int):
     return [max(res[i][k] for i in res) for k in range(n_steps)]
 
 
+def host_mem_available():
+    """MemAvailable of /proc/meminfo in bytes, or None where there is none."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
 def host_cores():
     try:
         aff = len(os.sched_getaffinity(0))
@@ -998,6 +1010,15 @@ def run_e2e(e, w, args, stream, n_params, t0):
     if need > free - (2 << 30):
         return {"value": None, "unit": "params/s",
                 "note": f"second device buffer set ({need / 1e9:.0f} GB) does not fit"}
+    # pinned host memory of every process on this node at once: leave most of
+    # the host's available memory alone
+    pinned = sum(x.numel() * 2 for G in e.gbufs for x in G) + (hi - lo) * 2
+    local_world = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    avail = host_mem_available()
+    if avail is not None and pinned * local_world > 0.6 * avail:
+        return {"value": None, "unit": "params/s",
+                "note": f"{local_world} x {pinned / 1e9:.0f} GB of pinned host buffers would "
+                        f"exceed 60% of the host's {avail / 1e9:.0f} GB available memory"}
     try:
         host_g = [[torch.empty(x.numel(), dtype=x.dtype, pin_memory=True) for x in G]
                   for G in e.gbufs]

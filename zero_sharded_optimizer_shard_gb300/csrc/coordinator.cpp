@@ -255,8 +255,17 @@ zero3_status prefetch_ahead(zero3_coordinator* c) {
     if (!c->trace_ok || c->cfg.prefetch_bucket_size <= 0) return ZERO3_OK;
     std::vector<int32_t> ks;
     std::vector<uint16_t*> outs;
+    std::vector<uint64_t> seqs;  // the release each taken range waits for
     uint64_t wait_seq = 0;
-    try {
+    const size_t most = c->trace.size() - static_cast<size_t>(c->pos);
+    try {  // no allocation after this: the loop below cannot throw
+        ks.reserve(most);
+        outs.reserve(most);
+        seqs.reserve(most);
+    } catch (const std::bad_alloc&) {
+        return ZERO3_ENOMEM;
+    }
+    {
         for (int64_t j = c->pos; j < static_cast<int64_t>(c->trace.size()); ++j) {
             const int32_t k = c->trace[j];
             if (c->off[k] >= 0) continue;  // already gathered (ahead, kept, or in this batch)
@@ -264,33 +273,51 @@ zero3_status prefetch_ahead(zero3_coordinator* c) {
             if (c->ahead_elems + n > c->cfg.prefetch_bucket_size) break;
             if (c->live + n > c->cfg.max_live_parameters) break;
             int64_t o = 0;
+            uint64_t seq = 0;
             if (n > 0) {
-                uint64_t seq = 0;
                 o = free_take(c, span_of(c, k), &seq);
                 if (o < 0) break;  // no room now: try again at the next fetch
                 wait_seq = std::max(wait_seq, seq);
             }
             ks.push_back(k);
             outs.push_back(c->arena + o);
+            seqs.push_back(seq);
             c->off[k] = o;
             c->live += n;
             c->status[k] = ZERO3_INFLIGHT;
             c->ahead[k] = 1;
             c->ahead_elems += n;
         }
-    } catch (const std::bad_alloc&) {
-        return ZERO3_ENOMEM;  // (ranges taken so far are accounted and stay valid)
     }
     if (ks.empty()) return ZERO3_OK;
+    // a batch that cannot be issued leaves nothing behind: its ranges return
+    // to the free list and its submodules to NOT_AVAILABLE
+    auto undo = [c, &ks, &seqs]() {
+        for (size_t i = 0; i < ks.size(); ++i) {
+            const int32_t k = ks[i];
+            const int64_t n = numel_of(c, k);
+            if (n > 0) free_insert(c, c->off[k], span_of(c, k), seqs[i]);
+            c->live -= n;
+            c->ahead_elems -= n;
+            c->ahead[k] = 0;
+            c->off[k] = -1;
+            c->status[k] = ZERO3_NOT_AVAILABLE;
+        }
+    };
     // release events of one stream complete in order: the latest covers all
     if (wait_seq > 0 &&
-        cudaStreamWaitEvent(c->prefetch, c->rel[wait_seq % kReleaseRing], 0) != cudaSuccess)
+        cudaStreamWaitEvent(c->prefetch, c->rel[wait_seq % kReleaseRing], 0) != cudaSuccess) {
+        undo();
         return ZERO3_ECUDA;
+    }
     int64_t launches = 0;
     zero3_status st = z3::gather_submodules(c->plan, ks.data(), static_cast<int64_t>(ks.size()),
                                             c->sparam.data(), c->persist, outs.data(), c->prefetch,
                                             &launches);
-    if (st != ZERO3_OK) return st;
+    if (st != ZERO3_OK) {
+        undo();
+        return st;
+    }
     const uint64_t seq = ++c->prefetch_seq;  // every event below marks this position
     for (int32_t k : ks) {
         if (cudaEventRecord(c->ready[k], c->prefetch) != cudaSuccess) return ZERO3_ECUDA;

@@ -401,7 +401,11 @@ zero3_status zero3_coordinator_create(zero3_plan* plan, const int32_t* trace, in
         c->ahead.assign(n_sub, 0);
         c->ready.assign(n_sub, nullptr);
         c->ready_seq.assign(n_sub, 0);
-        // only whole 8-element units of the arena are handed out
+        // only whole 8-element units of the arena are handed out.  Free
+        // ranges are separated by live ones, so there are at most n_sub + 1
+        // of them: with that capacity reserved, inserting never allocates
+        // (and never throws) later.
+        c->free_list.reserve(static_cast<size_t>(n_sub) + 2);
         if (arena_elems >= 8) c->free_list.push_back(FreeRange{0, arena_elems / 8 * 8, 0});
     } catch (const std::bad_alloc&) {
         delete c;

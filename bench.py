@@ -1112,6 +1112,7 @@ def run_e2e(e, w, args, stream, n_params, t0):
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms,
             "wall_ms_per_step": wall * 1e3 / steps,
             "upload_ms_per_step": up_ms,
+            "upload_ms_each": [round(a.elapsed_time(b_), 3) for a, b_ in up_t],
             "h2d_gbs": h2d_gbs,
             "h2d_link_gbs": link["h2d"], "d2h_link_gbs": link["d2h"],
             "h2d_frac": h2d_gbs / link["h2d"],

@@ -122,18 +122,27 @@ __device__ __forceinline__ float int8_code_f32(uint32_t biased_word, int k) {
     const uint32_t v = __byte_perm(biased_word, 0x4B000000u, 0x7650u | static_cast<uint32_t>(k));
     return __fsub_rn(__uint_as_float(v), 8388736.0f);  // 2^23 + 128
 }
-__device__ __forceinline__ float int4_code_f32(uint32_t biased_word, int k) {
-    const uint32_t v = ((biased_word >> (4 * k)) & 0xfu) | 0x4B000000u;
+// int4: the biased nibbles split once into two words of one nibble per byte
+// (even codes from the low nibbles, odd codes from the high ones), then the
+// same byte permute as int8.
+__device__ __forceinline__ float int4_code_f32(uint32_t nibble_bytes, int k) {
+    const uint32_t v = __byte_perm(nibble_bytes, 0x4B000000u, 0x7650u | static_cast<uint32_t>(k));
     return __fsub_rn(__uint_as_float(v), 8388616.0f);  // 2^23 + 8
 }
 
-// Code e (0..7) of a realigned unit as binary32.
+// The 8 codes of a realigned unit as binary32.
 template <int KIND>
-__device__ __forceinline__ float code_f32(const typename Unit<KIND>::T& u, int e) {
-    if constexpr (KIND == kPieceInt4)
-        return int4_code_f32(u ^ 0x88888888u, e);
-    else
-        return int8_code_f32((e < 4 ? u.x : u.y) ^ 0x80808080u, e & 3);
+__device__ __forceinline__ void codes_f32(const typename Unit<KIND>::T& u, float* f) {
+    if constexpr (KIND == kPieceInt4) {
+        const uint32_t x = u ^ 0x88888888u;
+        const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = int4_code_f32((e & 1) ? hi : lo, e >> 1);
+    } else {
+        const uint32_t x0 = u.x ^ 0x80808080u, x1 = u.y ^ 0x80808080u;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = int8_code_f32(e < 4 ? x0 : x1, e & 3);
+    }
 }
 
 // Destination element d of piece P, element by element (chunks at the
@@ -191,9 +200,9 @@ __device__ __forceinline__ void piece_phase2(uint16_t* dst, int64_t x0, int lane
             x = u;
         } else {
             float y[8];
+            codes_f32<KIND>(u, y);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                y[e] = __fmul_rn(code_f32<KIND>(u, e), e < split ? sc0[j] : sc1[j]);
+            for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(y[e], e < split ? sc0[j] : sc1[j]);
             x = pack8(y);
         }
         // plain stores: evict-first stores measured slower for the

@@ -242,6 +242,17 @@ template <int MAXP>
 zero3_status piece_flush(PieceArgs<MAXP>& a, int kind, cudaStream_t stream, int64_t* launches,
                          cudaError_t (*launch)(int, const PieceArgs<MAXP>&, cudaStream_t)) {
     if (a.n == 0) return ZERO3_OK;
+    // pieces were numbered at 128 chunks per warp; a phased dequantizing
+    // launch takes more per warp (fewer warps, so the 32-bit bound holds)
+    bool phased = false;
+    for (int i = 0; i < a.n; ++i) phased = phased || a.piece[i].ph != 0;
+    const uint64_t wc = static_cast<uint64_t>(piece_warp_chunks(kind, phased));
+    if (wc != 128) {
+        for (int i = 0; i < a.n; ++i) {
+            const uint64_t chunks = static_cast<uint64_t>((a.piece[i].hi + 7) / 8);
+            a.warp0[i + 1] = a.warp0[i] + static_cast<uint32_t>((chunks + wc - 1) / wc);
+        }
+    }
     const cudaError_t e = launch(kind, a, stream);
     a.n = 0;
     if (e != cudaSuccess) return ZERO3_ECUDA;
@@ -256,8 +267,9 @@ zero3_status piece_add(PieceArgs<MAXP>& a, int kind, cudaStream_t stream, int64_
                        cudaError_t (*launch)(int, const PieceArgs<MAXP>&, cudaStream_t),
                        const Piece& pc) {
     const uint64_t chunks = static_cast<uint64_t>((pc.hi + 7) / 8);
-    const uint64_t warps = (chunks + kPieceWarpChunks - 1) / kPieceWarpChunks;
-    const uint64_t cap = 0xffffffffull - kPieceWarpChunks;  // room for the grid rounding
+    const uint64_t wc = static_cast<uint64_t>(piece_warp_chunks(kind, false));
+    const uint64_t warps = (chunks + wc - 1) / wc;
+    const uint64_t cap = 0xffffffffull - 256;  // room for the grid rounding
     if (warps > cap) return ZERO3_EINVAL;  // a single piece beyond 2^41 elements
     if (a.n == MAXP || (a.n > 0 && a.warp0[a.n] + warps > cap)) {
         zero3_status st = piece_flush(a, kind, stream, launches, launch);

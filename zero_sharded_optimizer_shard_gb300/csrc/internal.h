@@ -111,11 +111,16 @@ struct Piece {
     int32_t pad_;
 };
 
-// A warp takes 128 consecutive chunks (1024 elements) of one piece; the
+// A warp takes consecutive chunks of one piece: 128 (1024 elements), or 192
+// in a dequantizing launch where some source is phased (such a warp's
+// per-warp set-up and its one extra source unit then weigh less per chunk;
+// its units are 8 or 4 bytes, so six per lane fit the registers).  The
 // launch's warps are numbered piece after piece.  warp0[i] is the first warp
 // of piece i and warp0[n] the launch's warp count, so the piece of a warp is
 // found by a binary search that every lane of the warp takes alike.
-constexpr int kPieceWarpChunks = 128;
+constexpr int piece_warp_chunks(int kind, bool phased) {
+    return kind != kPieceBf16 && phased ? 192 : 128;
+}
 constexpr int kSmallPieces = 64;    // one submodule, the all-gathers
 constexpr int kLargePieces = 512;   // several submodules in one launch
 template <int MAXP>

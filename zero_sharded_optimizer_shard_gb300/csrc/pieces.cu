@@ -22,23 +22,27 @@ namespace {
 // flight and no narrow or partial accesses.
 //
 // Chunks are aligned to the DESTINATION, so every store is one aligned
-// 16-byte store; a source at a nonzero phase is realigned on the way in.
-// A warp's 32 lanes hold 32 consecutive chunks of one piece (per step j of
-// the thread's four chunks), so lane l loads the aligned source unit under
-// its chunk and takes lane l+1's by shuffle (lane 31 loads the one after):
-// one aligned load per chunk.  Chunks whose source units would reach past
-// either end of the piece (at most two per piece edge) are copied element by
-// element.  Each lane issues all of its loads before its first store (the
-// compiler cannot move a load above a store through a possibly aliasing
-// pointer, which would leave one load in flight per lane).
-constexpr int kPieceChunks = kPieceWarpChunks / 32;   // chunks per lane
+// 16-byte store; a source at a nonzero phase is realigned on the way.  A
+// warp's 32 lanes hold 32 consecutive chunks of one piece per step j of the
+// lane's chunks (four, or six in a phased dequantizing launch), so lane l
+// loads the aligned source unit under its chunk and takes lane l+1's by
+// shuffle: one aligned load per chunk.  The copy realigns the loaded units
+// (lane 31 loads the unit after its own); a dequantizing warp first
+// dequantizes every unit and realigns the bf16 results.  Chunks whose source
+// units would reach past either end of the piece (at most two per piece
+// edge) are copied element by element.  Each lane issues all of its loads
+// before its first store (the compiler cannot move a load above a store
+// through a possibly aliasing pointer, which would leave one load in flight
+// per lane).
+template <int KIND, bool PHASED>
+constexpr int kLaneChunks = piece_warp_chunks(KIND, PHASED) / 32;  // chunks per lane
 
-// Source unit of a chunk and its realignment, per kind.
-//   bf16: 8 elements per aligned 16-byte unit; PH elements.
-//   int8: 8 codes per aligned 8-byte unit; PH bytes.
-//   int4: 8 codes per aligned 4-byte unit; PH nibbles.
-// The phase is the same for a whole piece, hence for a whole warp, so the
-// realignment is compiled per phase: a few funnel shifts of fixed words.
+// Source unit of a chunk, per kind: 8 bf16 elements in an aligned 16-byte
+// unit, 8 int8 codes in an aligned 8-byte unit, 8 int4 codes in an aligned
+// 4-byte unit.  Realignment always moves 8 bf16 values (the copy's units, or
+// dequantized ones) by PH elements; the phase is the same for a whole piece,
+// hence for a whole warp, so it is compiled per phase: a few funnel shifts
+// of fixed words.
 template <int KIND>
 struct Unit;
 template <>
@@ -80,19 +84,6 @@ struct Unit<kPieceInt8> {
     static __device__ __forceinline__ T load(const char* p) {
         return __ldcs(reinterpret_cast<const uint2*>(p));
     }
-    static __device__ __forceinline__ T shfl(const T& x) {
-        return make_uint2(__shfl_down_sync(0xffffffffu, x.x, 1),
-                          __shfl_down_sync(0xffffffffu, x.y, 1));
-    }
-    // bytes PH..PH+7 of the 16 bytes a, b
-    template <int PH>
-    static __device__ __forceinline__ T realign(const T& a, const T& b) {
-        const uint32_t w[4] = {a.x, a.y, b.x, b.y};
-        constexpr int k = PH / 4;
-        constexpr uint32_t sh = (PH & 3) * 8u;
-        if constexpr (sh == 0) return make_uint2(w[k], w[k + 1]);
-        return make_uint2(__funnelshift_r(w[k], w[k + 1], sh), __funnelshift_r(w[k + 1], w[k + 2], sh));
-    }
 };
 template <>
 struct Unit<kPieceInt4> {
@@ -105,44 +96,53 @@ struct Unit<kPieceInt4> {
     static __device__ __forceinline__ T load(const char* p) {
         return __ldcs(reinterpret_cast<const unsigned int*>(p));
     }
-    static __device__ __forceinline__ T shfl(const T& x) {
-        return __shfl_down_sync(0xffffffffu, x, 1);
-    }
-    template <int PH>
-    static __device__ __forceinline__ T realign(const T& a, const T& b) {
-        return __funnelshift_r(a, b, PH * 4u);
-    }
 };
 
 // Exact binary32 value of a code without a conversion instruction: the code
-// plus a bias (128 for int8, 8 for int4) is an integer below 2^8, placed in
-// the low mantissa bits of 2^23; subtracting 2^23 + bias is exact.
-__device__ __forceinline__ float int8_code_f32(uint32_t biased_word, int k) {
-    // byte k of the biased word under the exponent byte 0x4B (2^23)
-    const uint32_t v = __byte_perm(biased_word, 0x4B000000u, 0x7650u | static_cast<uint32_t>(k));
-    return __fsub_rn(__uint_as_float(v), 8388736.0f);  // 2^23 + 128
-}
-// int4: the biased nibbles split once into two words of one nibble per byte
-// (even codes from the low nibbles, odd codes from the high ones), then the
-// same byte permute as int8.
-__device__ __forceinline__ float int4_code_f32(uint32_t nibble_bytes, int k) {
-    const uint32_t v = __byte_perm(nibble_bytes, 0x4B000000u, 0x7650u | static_cast<uint32_t>(k));
-    return __fsub_rn(__uint_as_float(v), 8388616.0f);  // 2^23 + 8
+// plus a bias (128 for int8, 8 for int4) is an integer below 2^8; a byte
+// permute places byte k of a word of such biased codes in the low mantissa
+// bits of 2^23, and subtracting 2^23 + bias is exact.
+__device__ __forceinline__ float biased_code_f32(uint32_t byte_word, int k) {
+    return __uint_as_float(__byte_perm(byte_word, 0x4B000000u, 0x7650u | static_cast<uint32_t>(k)));
 }
 
-// The 8 codes of a realigned unit as binary32.
+// bf16_rne((a - K) * s) and bf16_rne((b - K) * s) as one packed bf16 pair:
+// the binary32 subtraction and multiplication, each rounded to nearest even,
+// issued as one two-lane instruction each (sub/mul .rn.f32x2).
+__device__ __forceinline__ uint32_t dequant_pair(float a, float b, float K, float s) {
+    float ya, yb;
+    asm("{\n\t.reg .b64 p, k, q;\n\t"
+        "mov.b64 p, {%2, %3};\n\tmov.b64 k, {%4, %4};\n\tsub.rn.f32x2 p, p, k;\n\t"
+        "mov.b64 q, {%5, %5};\n\tmul.rn.f32x2 p, p, q;\n\tmov.b64 {%0, %1}, p;\n\t}"
+        : "=f"(ya), "=f"(yb)
+        : "f"(a), "f"(b), "f"(K), "f"(s));
+    return pack_bf16x2(ya, yb);
+}
+
+// The 8 codes of an aligned source unit times their block scale s, as 8
+// bf16: y = bf16_rne(f32(code) * s).  Units start at multiples of 8 in the
+// shard and blocks at multiples of 256, so one scale serves the whole unit.
 template <int KIND>
-__device__ __forceinline__ void codes_f32(const typename Unit<KIND>::T& u, float* f) {
+__device__ __forceinline__ uint4 dequant_unit(const typename Unit<KIND>::T& u, float s) {
+    uint32_t w[4];
     if constexpr (KIND == kPieceInt4) {
+        // the biased nibbles split once into a word of the even codes (low
+        // nibbles) and one of the odd codes (high nibbles), one per byte
         const uint32_t x = u ^ 0x88888888u;
         const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = int4_code_f32((e & 1) ? hi : lo, e >> 1);
+        for (int k = 0; k < 4; ++k)
+            w[k] = dequant_pair(biased_code_f32(lo, k), biased_code_f32(hi, k), 8388616.0f, s);  // 2^23 + 8
     } else {
         const uint32_t x0 = u.x ^ 0x80808080u, x1 = u.y ^ 0x80808080u;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = int8_code_f32(e < 4 ? x0 : x1, e & 3);
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t x = k < 2 ? x0 : x1;
+            w[k] = dequant_pair(biased_code_f32(x, 2 * (k & 1)), biased_code_f32(x, 2 * (k & 1) + 1),
+                                8388736.0f, s);  // 2^23 + 128
+        }
     }
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Destination element d of piece P, element by element (chunks at the
@@ -164,50 +164,63 @@ __device__ __forceinline__ uint16_t piece_element(const Piece& P, int64_t d) {
     }
 }
 
-// Phase 2 of a warp's chunks at source phase PH: take the neighbour's unit
-// by shuffle (lane 31 loaded its own), realign, convert and store the vector
-// chunks.  Every lane of the warp calls this (the shuffles need all of
-// them).
-// Dequantizing kinds: y = bf16_rne(f32(code) * scale), with each element's
-// own 256-element block scale; only a chunk whose source starts in the last
-// 7 elements of a block (possible when PH != 0) straddles two blocks, and its
-// tail takes the second scale (a select per element: measured cheaper than a
-// fix-up branch, which the compiler predicates).
-template <int KIND, int PH>
-__device__ __forceinline__ void piece_phase2(uint16_t* dst, int64_t x0, int lane,
-                                             typename Unit<KIND>::T* cur,
-                                             const typename Unit<KIND>::T* nxt, const bool* vec,
-                                             const float* sc0, const float* sc1) {
-    using U = Unit<KIND>;
-    // elements of a chunk in its first block: all 8 unless a phased chunk's
-    // source starts in the block's last 7 elements (the same for the lane's
-    // four chunks, which lie 256 elements apart)
-    int split = 8;
-    if constexpr (PH != 0 && KIND != kPieceBf16) {
-        const uint32_t in_block = static_cast<uint32_t>(x0) % kQwzBlock;  // x0 >= 0
-        if (in_block > kQwzBlock - 8) split = static_cast<int>(kQwzBlock - in_block);
-    }
+// Phase 2 of the copy at source phase PH: take the neighbour's unit by
+// shuffle (lane 31 loaded its own), realign and store the vector chunks.
+// Every lane of the warp calls this (the shuffles need all of them).
+template <int PH>
+__device__ __forceinline__ void copy_phase2(uint16_t* dst, int lane, uint4* cur, const uint4* nxt,
+                                            const bool* vec) {
+    using U = Unit<kPieceBf16>;
 #pragma unroll
-    for (int j = 0; j < kPieceChunks; ++j) {
-        typename U::T u = cur[j];
+    for (int j = 0; j < kLaneChunks<kPieceBf16, false>; ++j) {
+        uint4 u = cur[j];
         if constexpr (PH != 0) {
-            const typename U::T n = U::shfl(cur[j]);
+            const uint4 n = U::shfl(cur[j]);
             u = U::template realign<PH>(cur[j], lane == 31 ? nxt[j] : n);
         }
         if (!vec[j]) continue;
-        uint4 x;
-        if constexpr (KIND == kPieceBf16) {
-            x = u;
-        } else {
-            float y[8];
-            codes_f32<KIND>(u, y);
+        *reinterpret_cast<uint4*>(dst + 256 * j) = u;
+    }
+}
+
+// Phase 2 of a dequantizing piece at source phase PH.  Each lane
+// dequantizes its own source units, then the bf16 results are realigned as
+// in the copy: a unit never straddles two 256-element scale blocks (a
+// realigned chunk can), so every unit takes one scale and no per-element
+// select.  A chunk at phase PH needs
+// its own unit and the next one: lane l's next unit is lane l + 1's of the
+// same step, lane 31's is lane 0's of the next step, and for the last step
+// lane 0's extra unit `ext` (the one after the warp's last).  One indexed
+// shuffle per word serves both cases: lane 0 offers its next step's value.
+template <int KIND, int C, int PH>
+__device__ __forceinline__ void dequant_phase2(uint16_t* dst, int lane,
+                                               const typename Unit<KIND>::T* cur, const float* sc,
+                                               const typename Unit<KIND>::T& ext, float sce,
+                                               const bool* vec) {
+    if constexpr (PH == 0) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(y[e], e < split ? sc0[j] : sc1[j]);
-            x = pack8(y);
+        for (int j = 0; j < C; ++j)
+            if (vec[j]) *reinterpret_cast<uint4*>(dst + 256 * j) = dequant_unit<KIND>(cur[j], sc[j]);
+    } else {
+        // each unit is dequantized just before the chunk that first needs
+        // it, so two dequantized units are live at a time
+        const int from = (lane + 1) & 31;
+        uint4 o = dequant_unit<KIND>(cur[0], sc[0]);
+#pragma unroll
+        for (int j = 0; j < C; ++j) {
+            // lane 0's next unit (the one after the warp's last for j = C-1)
+            const uint4 on = j + 1 < C ? dequant_unit<KIND>(cur[j + 1], sc[j + 1])
+                                       : dequant_unit<KIND>(ext, sce);
+            const uint4 give = lane == 0 ? on : o;
+            uint4 n;
+            n.x = __shfl_sync(0xffffffffu, give.x, from);
+            n.y = __shfl_sync(0xffffffffu, give.y, from);
+            n.z = __shfl_sync(0xffffffffu, give.z, from);
+            n.w = __shfl_sync(0xffffffffu, give.w, from);
+            const uint4 x = Unit<kPieceBf16>::template realign<PH>(o, n);
+            if (vec[j]) *reinterpret_cast<uint4*>(dst + 256 * j) = x;
+            o = on;
         }
-        // plain stores: evict-first stores measured slower for the
-        // dequantizing all-gather (0.71 against 0.66 ms at 1.3B)
-        *reinterpret_cast<uint4*>(dst + 256 * j) = x;
     }
 }
 
@@ -235,85 +248,122 @@ __global__ void __launch_bounds__(kThreads, PHASED ? 4 : 5)
     const int ph = PHASED ? P.ph : 0;
     // destination index of the warp's first element, and of the lane's chunk
     // at step 0 (step j adds 256: 32 lanes of 8 elements)
-    const int64_t wbase = static_cast<int64_t>(w - a.warp0[lo]) * (kPieceWarpChunks * 8);
+    constexpr int C = kLaneChunks<KIND, PHASED>;
+    constexpr int kWarpElems = 32 * C * 8;
+    const int64_t wbase = static_cast<int64_t>(w - a.warp0[lo]) * kWarpElems;
     const int64_t d00 = wbase + 8 * lane;
     const int64_t x0 = P.s0 + d00;  // its source index
     const char* src = U::at(P.src, x0 - ph);  // the aligned source unit under it
     constexpr int kStep = 32 * U::kUnitBytes;
-    typename U::T cur[kPieceChunks], nxt[kPieceChunks];
-    bool vec[kPieceChunks];
-    float sc0[kPieceChunks], sc1[kPieceChunks];
-    // Phase 1: every load of the vector chunks (codes or values, block
-    // scales).  A warp whose 1024 elements and the units around them lie
-    // inside the piece (nearly all warps) needs no per-chunk bounds.
-    const bool interior = wbase >= P.lo + 8 && wbase + kPieceWarpChunks * 8 + 8 <= P.hi;
-    if (interior) {
-#pragma unroll
-        for (int j = 0; j < kPieceChunks; ++j) {
-            vec[j] = true;
-            cur[j] = U::load(src + j * kStep);
-            if (PHASED && ph && lane == 31) nxt[j] = U::load(src + j * kStep + U::kUnitBytes);
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < kPieceChunks; ++j) {
-            // the source unit under the chunk starts at destination index b
-            const int64_t b = d00 + 256 * j - ph;
-            vec[j] = b >= P.lo && b + (ph ? 16 : 8) <= P.hi;
-            if (b >= P.lo && b + 8 <= P.hi) cur[j] = U::load(src + j * kStep);
-            if (PHASED && ph && lane == 31 && vec[j])
-                nxt[j] = U::load(src + j * kStep + U::kUnitBytes);
-        }
-    }
-    // Block scales of the vector chunks: the chunk's first element's block,
-    // and its last element's (the same one unless a phased chunk straddles
-    // two blocks).
-    if constexpr (KIND != kPieceBf16) {
+    bool vec[C];
+    uint16_t* dst = P.dst + d00;
+    // Phase 1: every load of the vector chunks (source units, block scales).
+    // A warp whose chunks and the units around them lie inside the piece
+    // (nearly all warps) needs no per-chunk bounds.
+    const bool interior = wbase >= P.lo + 8 && wbase + kWarpElems + 8 <= P.hi;
+    if constexpr (KIND == kPieceBf16) {
+        uint4 cur[C], nxt[C];
         if (interior) {
-            // x0 >= 0: the warp starts past the piece's first element
-            const float* s0p = P.scales + static_cast<uint64_t>(x0) / kQwzBlock;
-            const float* s1p = P.scales + static_cast<uint64_t>(x0 + 7) / kQwzBlock;
 #pragma unroll
-            for (int j = 0; j < kPieceChunks; ++j) {
-                sc0[j] = s0p[j];
-                if constexpr (PHASED) sc1[j] = s1p[j];
+            for (int j = 0; j < C; ++j) {
+                vec[j] = true;
+                cur[j] = U::load(src + j * kStep);
+                if (PHASED && ph && lane == 31) nxt[j] = U::load(src + j * kStep + U::kUnitBytes);
             }
         } else {
-            // x0 itself may lie before the piece (negative) on an edge lane;
-            // a vector chunk's own source index x0 + 256 j never does
 #pragma unroll
-            for (int j = 0; j < kPieceChunks; ++j) {
-                if (vec[j]) {
-                    const uint64_t xj = static_cast<uint64_t>(x0 + 256 * j);
-                    sc0[j] = P.scales[xj / kQwzBlock];
-                    if constexpr (PHASED) sc1[j] = P.scales[(xj + 7) / kQwzBlock];
+            for (int j = 0; j < C; ++j) {
+                // the source unit under the chunk starts at destination index b
+                const int64_t b = d00 + 256 * j - ph;
+                vec[j] = b >= P.lo && b + (ph ? 16 : 8) <= P.hi;
+                if (b >= P.lo && b + 8 <= P.hi) cur[j] = U::load(src + j * kStep);
+                if (PHASED && ph && lane == 31 && vec[j])
+                    nxt[j] = U::load(src + j * kStep + U::kUnitBytes);
+            }
+        }
+        // Phase 2: realign (per phase, warp-uniform) and store.
+        if constexpr (!PHASED) {
+            copy_phase2<0>(dst, lane, cur, nxt, vec);
+        } else {
+            switch (ph) {
+                case 0: copy_phase2<0>(dst, lane, cur, nxt, vec); break;
+                case 1: copy_phase2<1>(dst, lane, cur, nxt, vec); break;
+                case 2: copy_phase2<2>(dst, lane, cur, nxt, vec); break;
+                case 3: copy_phase2<3>(dst, lane, cur, nxt, vec); break;
+                case 4: copy_phase2<4>(dst, lane, cur, nxt, vec); break;
+                case 5: copy_phase2<5>(dst, lane, cur, nxt, vec); break;
+                case 6: copy_phase2<6>(dst, lane, cur, nxt, vec); break;
+                default: copy_phase2<7>(dst, lane, cur, nxt, vec); break;
+            }
+        }
+    } else {
+        // The lane's units at steps 0..3 start at source index xu + 256 j
+        // (xu is negative on some edge lanes, never where a unit is read);
+        // lane 0 also reads the unit after the warp's last when phased.
+        typename U::T cur[C], ext = {};
+        float sc[C], sce = 0.0f;
+        const int64_t xu = x0 - ph;
+        const bool want_ext = PHASED && ph != 0 && lane == 0;
+        if (interior) {
+            const float* sp = P.scales + static_cast<uint64_t>(xu) / kQwzBlock;  // xu > 0 here
+#pragma unroll
+            for (int j = 0; j < C; ++j) {
+                vec[j] = true;
+                cur[j] = U::load(src + j * kStep);
+                sc[j] = sp[j];
+            }
+            if (want_ext) {
+                ext = U::load(src + C * kStep);
+                sce = sp[C];
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < C; ++j) {
+                const int64_t b = d00 + 256 * j - ph;  // destination index of the unit's start
+                vec[j] = b >= P.lo && b + (ph ? 16 : 8) <= P.hi;
+                cur[j] = typename U::T{};
+                sc[j] = 0.0f;
+                if (b >= P.lo && b + 8 <= P.hi) {
+                    cur[j] = U::load(src + j * kStep);
+                    sc[j] = P.scales[static_cast<uint64_t>(xu + 256 * j) / kQwzBlock];
+                }
+            }
+            if (want_ext) {
+                const int64_t b = d00 + 256 * C - ph;
+                if (b >= P.lo && b + 8 <= P.hi) {
+                    ext = U::load(src + C * kStep);
+                    sce = P.scales[static_cast<uint64_t>(xu + 256 * C) / kQwzBlock];
                 }
             }
         }
-    }
-    uint16_t* dst = P.dst + d00;
-    if constexpr (!PHASED) {
-        piece_phase2<KIND, 0>(dst, x0, lane, cur, nxt, vec, sc0, sc1);
-    } else {
-        switch (ph) {  // warp-uniform
-            case 0: piece_phase2<KIND, 0>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
-            case 1: piece_phase2<KIND, 1>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
-            case 2: piece_phase2<KIND, 2>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
-            case 3: piece_phase2<KIND, 3>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
-            case 4: piece_phase2<KIND, 4>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
-            case 5: piece_phase2<KIND, 5>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
-            case 6: piece_phase2<KIND, 6>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
-            default: piece_phase2<KIND, 7>(dst, x0, lane, cur, nxt, vec, sc0, sc1); break;
+        if constexpr (!PHASED) {
+            dequant_phase2<KIND, C, 0>(dst, lane, cur, sc, ext, sce, vec);
+        } else {
+            switch (ph) {
+                case 0: dequant_phase2<KIND, C, 0>(dst, lane, cur, sc, ext, sce, vec); break;
+                case 1: dequant_phase2<KIND, C, 1>(dst, lane, cur, sc, ext, sce, vec); break;
+                case 2: dequant_phase2<KIND, C, 2>(dst, lane, cur, sc, ext, sce, vec); break;
+                case 3: dequant_phase2<KIND, C, 3>(dst, lane, cur, sc, ext, sce, vec); break;
+                case 4: dequant_phase2<KIND, C, 4>(dst, lane, cur, sc, ext, sce, vec); break;
+                case 5: dequant_phase2<KIND, C, 5>(dst, lane, cur, sc, ext, sce, vec); break;
+                case 6: dequant_phase2<KIND, C, 6>(dst, lane, cur, sc, ext, sce, vec); break;
+                default: dequant_phase2<KIND, C, 7>(dst, lane, cur, sc, ext, sce, vec); break;
+            }
         }
     }
     // Phase 3: the chunks at the piece's edges, element by element.  Kept out
     // of the load phase: with its stores between the loads, the loads of the
     // later chunks were no longer all in flight together (measured: the int8
     // dequantizing all-gather at 1.3B took 0.84 ms instead of 0.66 ms).
+    // A rolled loop over a mask of the lane's remaining chunks: unrolled, it
+    // kept phase 2's values alive across it and spilled.
     if (!interior) {
+        uint32_t todo = 0;
 #pragma unroll
-        for (int j = 0; j < kPieceChunks; ++j) {
-            if (vec[j]) continue;
+        for (int j = 0; j < C; ++j) todo |= vec[j] ? 0u : 1u << j;
+        while (todo) {
+            const int j = __ffs(todo) - 1;
+            todo &= todo - 1;
             const int64_t d0 = d00 + 256 * j;
             const int64_t e0 = d0 > P.lo ? d0 : P.lo;
             const int64_t e1 = d0 + 8 < P.hi ? d0 + 8 : P.hi;

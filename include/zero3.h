@@ -23,8 +23,11 @@
  *    but every thread waits for the previous grids to complete, and their
  *    writes to be visible, before it touches memory.  Plain stream order
  *    therefore holds for the data, whatever kernel (this library's or
- *    another's) comes before or after, and the calls can be captured in a
- *    CUDA graph.
+ *    another's) comes before or after.  The compute calls (steps,
+ *    reduce-scatter, all-gathers, quantization) can be captured in a CUDA
+ *    graph; the fetch, release and coordinator calls keep host-side state
+ *    (status, references, events) that a replay would not repeat, so they
+ *    are issued directly.
  *  - A plan is owned by the library: created by zero3_partition, released by
  *    zero3_plan_destroy.  Calls on one plan must not run concurrently from
  *    several host threads.

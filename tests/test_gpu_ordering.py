@@ -156,3 +156,49 @@ def test_fused_step_replays_from_a_cuda_graph(dev):
         assert np.array_equal(v1.cpu().numpy().view(np.uint32), st.v[1].view(np.uint32)), k
         assert np.array_equal(u16(f), O.allgather(plan, st.sparam)), k
         assert np.array_equal(u16(pp), ps.param), k
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_qwz_step_and_dequantizing_gather_replay_from_a_cuda_graph(dev, bits):
+    """The qwZ step and the dequantizing all-gather (a piece launch whose
+    sources sit at nonzero phases: the ragged list at N_d = 7) captured once
+    in a CUDA graph and replayed three times equal three oracle steps with the
+    same step count and gradients, codes and gathered bf16 bit for bit."""
+    from tests._oracle_runs import host_grads, host_master
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    w = W.ragged_small(7)
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    e, s = emu(w)
+    assert e.S % 8 != 0  # the shards start at nonzero phases in the flat buffer
+    nb = -(-e.S // 256)
+    codes = [torch.zeros(max(e.S, 16), dtype=torch.int8, device=dev) for _ in range(e.nd)]
+    scales = [torch.zeros(max(nb, 4), dtype=torch.float32, device=dev) for _ in range(e.nd)]
+    with torch.cuda.stream(s):
+        e.fill_grads(1)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        zero3.zero3_step_qwz(e.plan, e.hp, 1, e.ptrs(e.grads[0]), 0, e.ptrs(e.master), e.ptrs(e.m),
+                             e.ptrs(e.v), e.ptrs(e.sparam), e.ptrs(codes), e.ptrs(scales), None,
+                             0, e.psi_pad, e.sid, bits=bits)
+        zero3.zero3_allgather_qwz(e.plan, e.ptrs(codes), e.ptrs(scales), e.full.data_ptr(), 0,
+                                  e.psi_pad, e.sid, bits=bits)
+    torch.cuda.synchronize()
+    snaps = []
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g.replay()
+            snaps.append(([m.clone() for m in e.master], e.full.clone()))
+    torch.cuda.synchronize()
+    mf, mp = host_master(w, plan)
+    st, full, _ = O.init_state(plan, mf, mp)
+    G = host_grads(w, plan, 1)
+    for k in range(3):
+        O.sharded_step(plan, w.hparams, 1, G, st, full)
+        q = [O.qwz_quantize(st.sparam[r], bits=bits) for r in range(w.n_ranks)]
+        want = O.qwz_allgather(plan, [c for c, _ in q], [sc for _, sc in q])
+        masters, f = snaps[k]
+        for r in range(w.n_ranks):
+            assert np.array_equal(masters[r].cpu().numpy().view(np.uint32),
+                                  st.master[r].view(np.uint32)), (k, r)
+        assert np.array_equal(u16(f), want), k

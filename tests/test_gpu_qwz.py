@@ -120,3 +120,47 @@ def test_qwz_rejects_other_widths():
             zero3.zero3_quantize_shards(e.plan, e.ptrs(e.sparam), e.ptrs(codes), e.ptrs(scales), 0,
                                         e.psi_pad, e.sid, bits=b)
         assert exc.value.status == zero3.EINVAL
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("wname", ["ragged7", "mini8"])
+def test_dequantizing_gather_of_sub_ranges(wname, bits):
+    """The dequantizing all-gather over many sub-ranges of the flat buffer:
+    the whole range, single elements, ranges around every rank boundary,
+    ranges ending 1..2053 elements after a shard's start or before its end
+    (the last source units of a piece), and seeded random ranges.  On the
+    ragged list at N_d = 7 (S mod 8 = 5) every launch has phased sources;
+    at N_d = 8 they are aligned.  Each range equals the oracle's whole gather
+    there, bit for bit, and no element outside it is written."""
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+    w = {"ragged7": lambda: W.ragged_small(7), "mini8": lambda: W.mini_gpt(8)}[wname]()
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    e = Emulation(w)
+    e.init_params()
+    codes, scales = wire(e)
+    zero3.zero3_quantize_shards(e.plan, e.ptrs(e.sparam), e.ptrs(codes), e.ptrs(scales), 0,
+                                e.psi_pad, e.sid, bits=bits)
+    torch.cuda.synchronize()
+    q = [O.qwz_quantize(u16(e.sparam[r]), bits=bits) for r in range(e.nd)]
+    want = O.qwz_allgather(plan, [c for c, _ in q], [s for _, s in q])
+    S, N = e.S, e.psi_pad
+    ranges = [(0, N), (0, 1), (N - 1, N)]
+    for r in range(e.nd):
+        b0, b1 = r * S, (r + 1) * S
+        ranges += [(b0 - 9, b0 + 9), (b0 - 1, b0 + 1), (b0 - 3, b0), (b0, b0 + 5)]
+        ranges += [(b0, b0 + d) for d in (1, 7, 8, 9, 2053)]
+        ranges += [(b1 - d, b1) for d in (1, 7, 8, 9, 2053)]
+    rng = np.random.default_rng(7)
+    for _ in range(24):
+        lo = int(rng.integers(0, N))
+        ranges.append((lo, lo + int(rng.integers(1, 5000))))
+    ranges = sorted({(max(0, lo), min(N, hi)) for lo, hi in ranges if min(N, hi) > max(0, lo)})
+    for lo, hi in ranges:
+        e.full.view(torch.int16).fill_(0x7FC1)
+        zero3.zero3_allgather_qwz(e.plan, e.ptrs(codes), e.ptrs(scales), e.full.data_ptr(), lo,
+                                  hi, e.sid, bits=bits)
+        torch.cuda.synchronize()
+        got = u16(e.full)
+        assert np.array_equal(got[lo:hi], want[lo:hi]), (lo, hi)
+        assert (got[:lo] == 0x7FC1).all() and (got[hi:] == 0x7FC1).all(), (lo, hi)

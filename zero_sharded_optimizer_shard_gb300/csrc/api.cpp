@@ -699,9 +699,11 @@ zero3_status zero3_fetch_submodules(zero3_plan* p, const int32_t* ks, int32_t n,
     zero3_status st = z3::gather_submodules(p, gather.data(), static_cast<int64_t>(gather.size()),
                                             sparam, persist_param, gather_out.data(), stream);
     if (st != ZERO3_OK) return st;
+    // every event first: a failed call leaves every status and count as it was
+    for (int32_t k : gather)
+        if (cudaEventRecord(p->events[k], stream) != cudaSuccess) return ZERO3_ECUDA;
     for (size_t j = 0; j < gather.size(); ++j) {
         const int32_t k = gather[j];
-        if (cudaEventRecord(p->events[k], stream) != cudaSuccess) return ZERO3_ECUDA;
         p->status[k] = ZERO3_INFLIGHT;
         p->refs[k] = 0;
         p->fetched_out[k] = gather_out[j];

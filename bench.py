@@ -996,8 +996,9 @@ def run_e2e(e, w, args, stream, n_params, t0):
     ranks' range of the full bf16 buffer) back into pinned host memory.
     Pipelined over two device buffer sets: the upload of step k+1 and the
     read-back of step k run on their own streams while step k computes;
-    events order every reuse of a buffer.  Before the pipelined run, the
-    same copies alone measure the host link (one copy per buffer)."""
+    events order every reuse of a buffer.  Two untimed pipelined steps come
+    before the timed ones.  Before the pipelined run, the same copies alone
+    measure the host link (one copy per buffer)."""
     import torch
     from zero_sharded_optimizer_shard_gb300 import zero3
     steps = max(2, min(args.steps, 6))
@@ -1057,12 +1058,16 @@ def run_e2e(e, w, args, stream, n_params, t0):
             torch.cuda.synchronize()
             ts.append(a_.elapsed_time(b_))
         link[nm] = nb / (min(ts) / 1e3) / 1e9
+    # untimed pipelined steps first: the timed region starts in the steady
+    # state, not with the first upload after the link probe's idle gap
+    warm = 2
+    total = warm + steps
     ev = lambda: torch.cuda.Event()
-    uploaded = [ev() for _ in range(steps)]
+    uploaded = [ev() for _ in range(total)]
     up_t = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(steps)]
-    computed = [ev() for _ in range(steps)]
-    read = [ev() for _ in range(steps)]
+            for _ in range(total)]
+    computed = [ev() for _ in range(total)]
+    read = [ev() for _ in range(total)]
     # one copy stream: every copy in issue order (upload k+1, then read-back
     # k); two: read-backs on their own stream, concurrent with uploads
     down_s = up if args.e2e_copy_streams == 1 else down
@@ -1080,9 +1085,16 @@ def run_e2e(e, w, args, stream, n_params, t0):
     t = t0
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.perf_counter()
-    start.record(up)
+
+    def begin_timing():  # on the upload stream, right before step `warm`'s upload
+        nonlocal wall0
+        start.record(up)
+        wall0 = time.perf_counter()
+
+    if warm == 0:
+        begin_timing()
     enqueue_upload(0)
-    for k in range(steps):
+    for k in range(total):
         b = k % 2
         stream.wait_event(uploaded[k])
         if k >= 2:
@@ -1096,7 +1108,9 @@ def run_e2e(e, w, args, stream, n_params, t0):
                              e.ptrs(e.v), e.ptrs(e.sparam), dev_full[b].data_ptr(),
                              ps if c == 0 else None, clo, chi, e.sid)
         computed[k].record(stream)
-        if k + 1 < steps:
+        if k + 1 < total:
+            if k + 1 == warm:
+                begin_timing()
             enqueue_upload(k + 1)               # overlaps step k
         with torch.cuda.stream(down_s):
             down_s.wait_event(computed[k])
@@ -1106,10 +1120,11 @@ def run_e2e(e, w, args, stream, n_params, t0):
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     ms = start.elapsed_time(end) / steps
+    up_t = up_t[warm:]
     up_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in up_t)
     h2d_gbs = h2d / (up_ms / 1e3) / 1e9
     return {"value": n_params / (ms / 1e3), "unit": "params/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms,
+            "d2h_bytes_per_step": d2h, "steps": steps, "warmup": warm, "ms_per_step": ms,
             "wall_ms_per_step": wall * 1e3 / steps,
             "upload_ms_per_step": up_ms,
             "upload_ms_each": [round(a.elapsed_time(b_), 3) for a, b_ in up_t],

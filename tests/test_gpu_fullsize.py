@@ -219,6 +219,58 @@ def test_decoder_1p3b_bench_configuration():
     check_fetch_many(e, plan, w, T, 1, [groups[0], groups[-1]], lambda i: ps.param[i])
 
 
+@pytest.mark.parametrize("nbits", [8, 4])
+def test_decoder_1p3b_qwz_bench_configuration(nbits):
+    """The qwZ benchmark's launch configuration at full size: the 1.3B list at
+    N_d = 8, one quantizing fused step over the whole flat range, then the
+    dequantizing all-gather, three steps on the same gradients.  Sampled
+    256-element blocks (random ones and every rank's first and last, the
+    last one partial where S is not a multiple of 256): the packed codes, the
+    block scale and the gathered bf16 equal the oracle's quantization of the
+    oracle's step there, bit for bit."""
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+    w = W.decoder_1p3b()
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    e = Emulation(w, bucketed=False)
+    e.init_params()
+    e.fill_grads(1)
+    S, nd, blk = e.S, e.nd, 256
+    nb = -(-S // blk)
+    codes = [torch.empty(-(-S * nbits // 8), dtype=torch.int8, device="cuda") for _ in range(nd)]
+    scales = [torch.empty(nb, dtype=torch.float32, device="cuda") for _ in range(nd)]
+    lo, hi = e.chunks[0]
+    T = 3
+    for t in range(1, T + 1):
+        zero3.zero3_step_qwz(e.plan, e.hp, t, e.ptrs(e.grads[0]), lo, e.ptrs(e.master),
+                             e.ptrs(e.m), e.ptrs(e.v), e.ptrs(e.sparam), e.ptrs(codes),
+                             e.ptrs(scales), None, lo, hi, e.sid, bits=nbits)
+        zero3.zero3_allgather_qwz(e.plan, e.ptrs(codes), e.ptrs(scales), e.full.data_ptr(), lo,
+                                  hi, e.sid, bits=nbits)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(11 + nbits)
+    blocks = {(r, b) for r in range(nd) for b in (0, nb - 1)}
+    blocks |= {(int(rng.integers(0, nd)), int(rng.integers(0, nb))) for _ in range(400)}
+    blocks = sorted(blocks)
+    spans = [(r, b, r * S + b * blk, r * S + min((b + 1) * blk, S)) for r, b in blocks]
+    idx = np.concatenate([np.arange(f0, f1, dtype=np.int64) for _, _, f0, f1 in spans])
+    _, _, _, h = sampled_oracle(w, plan, idx, T, grad_step=1)
+    got_full = u16(e.full[torch.from_numpy(idx).to(e.full.device)])
+    want_full = np.empty_like(h)
+    pos = 0
+    for r, b, f0, f1 in spans:
+        n = f1 - f0
+        c, sc = O.qwz_quantize(h[pos:pos + n], bits=nbits)
+        want_full[pos:pos + n] = O.qwz_dequantize(c, sc)
+        packed = O.qwz_pack(c, nbits)
+        b0 = b * blk * nbits // 8
+        got_codes = codes[r][b0:b0 + packed.size].cpu().numpy().view(np.uint8)
+        assert np.array_equal(got_codes, packed), (r, b)
+        assert np.array_equal(bits(f32(scales[r][b:b + 1])), bits(sc[:1])), (r, b)
+        pos += n
+    assert np.array_equal(got_full, want_full)
+
+
 def test_llama_7b_rank0_view():
     """Rank 0's state only, gradients in 5e8-element bucket buffers (two
     launches per step), bf16 all-gather into the 6.7B-element full buffer."""

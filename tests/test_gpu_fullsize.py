@@ -271,6 +271,42 @@ def test_decoder_1p3b_qwz_bench_configuration(nbits):
     assert np.array_equal(got_full, want_full)
 
 
+def test_decoder_1p3b_stage12_bench_configuration():
+    """The ZeRO-1/2 benchmark's launch configuration at full size: the 1.3B
+    list at N_d = 8, every rank holding full bf16 parameters, one fused launch
+    over the whole flat range writing all eight copies, three steps on the
+    same gradients.  Sampled flat indices (random, shard, tensor and padding
+    edges): every rank's fp32 state and every rank's copy of the parameter
+    equal the oracle's step there, bit for bit."""
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+    w = W.decoder_1p3b()
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    e = Emulation(w, bucketed=False)
+    e.init_params()
+    e.fill_grads(1)
+    params = [e.full.clone() for _ in range(w.n_ranks)]
+    lo, hi = e.chunks[0]
+    T = 3
+    for t in range(1, T + 1):
+        zero3.zero3_step_stage12(e.plan, e.hp, t, e.ptrs(e.grads[0]), lo, e.ptrs(e.master),
+                                 e.ptrs(e.m), e.ptrs(e.v), [x.data_ptr() for x in params],
+                                 lo, hi, e.sid)
+    torch.cuda.synchronize()
+    idx = sample_indices(plan, 0, plan.psi_pad, 60_000, 5)
+    p, m, v, h = sampled_oracle(w, plan, idx, T, grad_step=1)
+    S = plan.shard_len
+    r, i = idx // S, idx % S
+    for q in np.unique(r):
+        sel = r == q
+        ii = torch.from_numpy(i[sel]).to(e.master[q].device)
+        for name, buf, ref in (("master", e.master[q], p), ("m", e.m[q], m), ("v", e.v[q], v)):
+            assert np.array_equal(bits(f32(buf[ii])), bits(ref[sel])), (name, q)
+    ti = torch.from_numpy(idx).to(params[0].device)
+    for q in range(w.n_ranks):
+        assert np.array_equal(u16(params[q][ti]), h), q
+
+
 def test_llama_7b_rank0_view():
     """Rank 0's state only, gradients in 5e8-element bucket buffers (two
     launches per step), bf16 all-gather into the 6.7B-element full buffer."""

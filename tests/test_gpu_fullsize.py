@@ -307,6 +307,33 @@ def test_decoder_1p3b_stage12_bench_configuration():
         assert np.array_equal(u16(params[q][ti]), h), q
 
 
+def test_decoder_1p3b_unfused_bench_configuration():
+    """The unfused ablation's launch configuration at full size: the 1.3B
+    list at N_d = 8, fp32 reduce-scatter into per-rank shard gradients, the
+    AdamW launch, the all-gather launch, each over the whole flat range, two
+    steps on the same gradients.  Sampled indices: states, shards and the
+    gathered buffer equal the oracle's step, bit for bit (the fp32 unfused
+    path computes exactly what the fused step computes)."""
+    from zero_sharded_optimizer_shard_gb300 import zero3
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+    w = W.decoder_1p3b()
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    e = Emulation(w, bucketed=False)
+    e.init_params()
+    e.fill_grads(1)
+    sg = [torch.empty(e.S, dtype=torch.float32, device="cuda") for _ in range(e.nd)]
+    lo, hi = e.chunks[0]
+    T = 2
+    for t in range(1, T + 1):
+        zero3.zero3_reduce_scatter(e.plan, e.ptrs(e.grads[0]), lo, lo, hi, e.ptrs(sg), zero3.F32,
+                                   e.sid)
+        zero3.zero3_adamw_step(e.plan, e.hp, t, e.ptrs(sg), zero3.F32, e.ptrs(e.master),
+                               e.ptrs(e.m), e.ptrs(e.v), e.ptrs(e.sparam), lo, hi, e.sid)
+        zero3.zero3_allgather(e.plan, e.ptrs(e.sparam), e.full.data_ptr(), lo, hi, e.sid)
+    torch.cuda.synchronize()
+    check_sample(e, plan, w, sample_indices(plan, 0, plan.psi_pad, 60_000, 6), T, grad_step=1)
+
+
 def test_llama_7b_rank0_view():
     """Rank 0's state only, gradients in 5e8-element bucket buffers (two
     launches per step), bf16 all-gather into the 6.7B-element full buffer."""

@@ -334,6 +334,68 @@ def test_decoder_1p3b_unfused_bench_configuration():
     check_sample(e, plan, w, sample_indices(plan, 0, plan.psi_pad, 60_000, 6), T, grad_step=1)
 
 
+def test_decoder_1p3b_coordinator_bench_configuration():
+    """The prefetching coordinator in its benchmark configuration at full
+    size: the 1.3B list, the forward-then-backward trace over every
+    submodule, an arena of three times the largest submodule, two steps'
+    traces with the step boundary between them.  After every fetch, sampled
+    positions of the gathered copy (and its ends) are read on the compute
+    stream before the release; each equals the oracle's bf16 parameter of
+    that element (the initial parameters: no optimizer step runs)."""
+    from zero_sharded_optimizer_shard_gb300 import synth, zero3
+    from zero_sharded_optimizer_shard_gb300.emulation import Emulation
+    from zero_sharded_optimizer_shard_gb300.workloads import STREAM_MASTER
+    w = W.decoder_1p3b()
+    plan = O.partition(w.numels, w.submodule_of, w.n_ranks, w.threshold, w.bucket)
+    e = Emulation(w, bucketed=False)
+    e.init_params()
+    n_sub = e.plan.info.n_submodules
+    sizes = [e.plan.submodule(k)[1] for k in range(n_sub)]
+    trace = list(range(n_sub)) + list(reversed(range(n_sub)))
+    arena_elems = (3 * max(sizes) + 7) // 8 * 8
+    arena = torch.empty(arena_elems, dtype=torch.bfloat16, device="cuda")
+    compute, prefetch = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    co = zero3.Coordinator(e.plan, trace, e.ptrs(e.sparam), e.pparam.data_ptr(), arena.data_ptr(),
+                           arena_elems, prefetch_bucket_size=w.bucket,
+                           max_live_parameters=arena_elems, max_reuse_distance=10**9,
+                           compute_stream=compute.cuda_stream,
+                           prefetch_stream=prefetch.cuda_stream)
+    rng = np.random.default_rng(9)
+    pers_init = O.cast_bf16(host_master_persist(w, plan))
+    snaps = []
+    for _ in range(2):
+        for k in trace:
+            members = [t for t in plan.submodules.get(k, []) if plan.numel[t] > 0]
+            pos, want = [], []
+            base = 0
+            for t in members:
+                nt = plan.numel[t]
+                js = np.unique(np.concatenate([rng.integers(0, nt, 300), [0, nt - 1]]))
+                pos.append(base + js)
+                if plan.persistent[t]:
+                    want.append(pers_init[plan.offset[t] + js])
+                else:
+                    want.append(O.bf16_rne(synth.normal_f32(w.seed, STREAM_MASTER, 0, 0,
+                                                            plan.offset[t] + js, w.master_sigma)))
+                base += nt
+            ptr = co.fetch(k)
+            if pos:
+                pos = np.concatenate(pos)
+                off = (ptr - arena.data_ptr()) // 2
+                ti = torch.from_numpy(off + pos).to(arena.device)
+                with torch.cuda.stream(compute):
+                    snaps.append((k, arena[ti], np.concatenate(want)))
+            co.release(k)
+        co.next_step()
+    torch.cuda.synchronize()
+    stats = co.stats()
+    del co
+    assert stats["prefetched"] > 0
+    for k, got, want in snaps:
+        assert np.array_equal(u16(got), want), f"submodule {k}"
+
+
 def test_llama_7b_rank0_view():
     """Rank 0's state only, gradients in 5e8-element bucket buffers (two
     launches per step), bf16 all-gather into the 6.7B-element full buffer."""

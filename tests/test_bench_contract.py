@@ -140,3 +140,30 @@ def test_fused_profile_matches_the_current_sources():
     alg_1p3b = 1_315_080_192 * 44 + 643_072 * 42
     assert 0.95 < bench.profile_traffic("decoder_1p3b", bench.kernels_sha()) / alg_1p3b < 1.02
     assert bench.profile_traffic("decoder_1p3b", "0" * 16) is None
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mode", [
+    ("--qwz",), ("--qwz", "--qwz-bits", "4"), ("--stage", "2"), ("--unfused",),
+    ("--coordinator", "--tokens", "256"), ("--workload", "ragged", "--no-e2e", "--no-cpu-baseline"),
+])
+def test_other_modes_print_a_line(mode):
+    """The bench's other measurement modes on the GPT-2-small list (the
+    ragged list for its own mode): each exits 0 and prints one JSON line with
+    positive timings."""
+    args = list(mode)
+    if "--workload" not in args:
+        args += ["--workload", "gpt2_small"]
+    d = run_bench(*args, "--steps", "2", "--warmup", "1")
+    if "--qwz" in mode:
+        assert d["fused_qwz"]["gbs"] > 0 and d["allgather_qwz"]["gbs"] > 0
+        assert d["config"]["workload"].endswith(f"qwZ int{mode[-1] if len(mode) > 1 else 8} "
+                                                "all-gather (block 256)")
+    elif "--unfused" in mode:
+        assert all(d["kernels"][k]["ms"] > 0 for k in ("reduce_scatter", "adamw", "allgather",
+                                                       "fused"))
+    elif "--coordinator" in mode:
+        assert set(d["modes"]) == {"prefetch", "on_demand", "gemm_only"}
+        assert d["modes"]["prefetch"]["stats"]["prefetched"] > 0
+    else:
+        assert d["value"] > 0 and d["ms_per_step"] > 0
